@@ -1,0 +1,239 @@
+"""Single-GPU MoE expert-parallel token shuffle for GB300: Python binding.
+
+A thin ctypes layer over the C ABI in include/ep.h (libep.so, hand-written
+CUDA for sm_103a).  It only marshals arguments: it allocates output tensors
+with torch and passes raw device pointers and the current CUDA stream.  Every
+step of layout, dispatch and combine runs in the library's kernels.  There is
+no CPU or PyTorch fallback.  If the library is missing or cannot be loaded,
+every call raises.
+
+The three steps follow the high-throughput expert-parallel kernels of
+"[Not ready] MSCCLPP EP implementation" (mscclpp pull request 852), section
+"Scope" (get_dispatch_layout, intranode_dispatch, intranode_combine), with the
+kUseFP8 payload cast of its low-latency dispatch.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libep.so")
+
+EP_OK = 0
+EP_ERRBIT_BAD_EXPERT = 1
+EP_ERRBIT_CAPACITY = 2
+EP_ERRBIT_TIMEOUT = 4
+EP_MAX_RANKS = 64
+EP_MAX_TOPK = 32
+EP_MAX_EXPERTS = 4096
+
+# every entry point declared in include/ep.h
+EXPORTED = ("ep_status_string", "ep_workspace_bytes", "ep_get_dispatch_layout",
+            "ep_layout_total_rows", "ep_dispatch", "ep_combine")
+
+_lib = None
+
+
+class EPError(RuntimeError):
+    pass
+
+
+def load(path: str | None = None) -> C.CDLL:
+    """Load libep.so (built by combine_get_dispatch_04_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise EPError(f"CUDA library not built: {path} is missing "
+                      "(run combine_get_dispatch_04_gb300.build.build())")
+    L = C.CDLL(path)
+    P, i32, i64, sz = C.c_void_p, C.c_int, C.c_int64, C.c_size_t
+    L.ep_status_string.argtypes = [i32]
+    L.ep_status_string.restype = C.c_char_p
+    L.ep_workspace_bytes.argtypes = [i64, i32, i32]
+    L.ep_workspace_bytes.restype = sz
+    L.ep_get_dispatch_layout.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
+    L.ep_layout_total_rows.argtypes = [P, i32, P, P]
+    L.ep_dispatch.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, i64, i32, P, P, P, P, P,
+                              P, P, P]
+    L.ep_combine.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, P, P]
+    for name in ("ep_get_dispatch_layout", "ep_layout_total_rows", "ep_dispatch", "ep_combine"):
+        getattr(L, name).restype = i32
+    _lib = L
+    return L
+
+
+def lib() -> C.CDLL:
+    return load()
+
+
+def _check(status: int, what: str):
+    if status != EP_OK:
+        msg = lib().ep_status_string(status).decode()
+        raise EPError(f"{what} failed: {msg}")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device):
+    return C.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None):
+    if not t.is_cuda:
+        raise EPError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise EPError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise EPError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise EPError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+@dataclass
+class Layout:
+    """Outputs of get_dispatch_layout (all on the device)."""
+    num_tokens_per_rank: torch.Tensor    # [R, R] int32, row = source rank
+    num_tokens_per_expert: torch.Tensor  # [R, E] int32, row = source rank
+    is_token_in_rank: torch.Tensor       # [T, R] bool
+    slot: torch.Tensor                   # [T, R] int32, -1 = not sent
+    recv_base: torch.Tensor              # [R + 1] int32, recv_base[R] = P
+    num_experts: int
+    num_ranks: int
+    workspace: torch.Tensor | None = None
+
+    @property
+    def num_tokens(self) -> int:
+        return self.slot.shape[0]
+
+
+def workspace_bytes(num_tokens: int, num_ranks: int, num_experts: int) -> int:
+    return int(lib().ep_workspace_bytes(num_tokens, num_ranks, num_experts))
+
+
+def alloc_layout(num_tokens: int, num_experts: int, num_ranks: int,
+                 device: torch.device) -> Layout:
+    T, R, E = num_tokens, num_ranks, num_experts
+    i32 = dict(dtype=torch.int32, device=device)
+    ws = torch.empty(max(workspace_bytes(T, R, E), 16), dtype=torch.uint8, device=device)
+    return Layout(torch.empty((R, R), **i32), torch.empty((R, E), **i32),
+                  torch.empty((T, R), dtype=torch.bool, device=device),
+                  torch.empty((T, R), **i32), torch.empty(R + 1, **i32), E, R, ws)
+
+
+def get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int, *,
+                        err: torch.Tensor | None = None, out: Layout | None = None) -> Layout:
+    """Per-rank / per-expert counts, is_token_in_rank and the slot of every
+    (token, destination rank) pair.  Enqueued on the current stream."""
+    _need(topk_idx, "topk_idx", torch.int64)
+    if topk_idx.dim() != 2:
+        raise EPError("topk_idx must be [num_tokens, num_topk]")
+    T, K = topk_idx.shape
+    L = out if out is not None else alloc_layout(T, num_experts, num_ranks, topk_idx.device)
+    if err is not None:
+        _need(err, "err", torch.int32)
+    _check(lib().ep_get_dispatch_layout(
+        _ptr(topk_idx), T, K, num_experts, num_ranks, _ptr(L.num_tokens_per_rank),
+        _ptr(L.num_tokens_per_expert), _ptr(L.is_token_in_rank), _ptr(L.slot),
+        _ptr(L.recv_base), _ptr(err), _ptr(L.workspace),
+        L.workspace.numel() if L.workspace is not None else 0, _stream(topk_idx.device)),
+        "ep_get_dispatch_layout")
+    return L
+
+
+def total_rows(layout: Layout) -> int:
+    """P = rows of the receive buffer (copies one int32 and synchronises)."""
+    v = C.c_int32(0)
+    _check(lib().ep_layout_total_rows(_ptr(layout.recv_base), layout.num_ranks, C.byref(v),
+                                      _stream(layout.recv_base.device)), "ep_layout_total_rows")
+    return int(v.value)
+
+
+@dataclass
+class Dispatched:
+    recv_x: torch.Tensor                # [cap, H] bf16, or [cap, H] uint8 E4M3 codes
+    recv_scales: torch.Tensor | None    # [cap, H/128] float32 (FP8 only)
+    recv_src_idx: torch.Tensor          # [cap] int32
+    recv_topk_idx: torch.Tensor         # [cap, K] int64
+    recv_topk_weights: torch.Tensor     # [cap, K] float32
+    num_recv_tokens_per_expert: torch.Tensor  # [R, E/R] int32
+    use_fp8: bool
+
+
+def worst_case_rows(num_tokens: int, num_topk: int, num_ranks: int) -> int:
+    return num_tokens * min(num_topk, num_ranks)
+
+
+def alloc_dispatched(capacity: int, hidden: int, num_topk: int, num_experts: int,
+                     num_ranks: int, use_fp8: bool, device: torch.device) -> Dispatched:
+    if use_fp8:
+        recv_x = torch.empty((capacity, hidden), dtype=torch.uint8, device=device)
+        scales = torch.empty((capacity, hidden // 128), dtype=torch.float32, device=device)
+    else:
+        recv_x = torch.empty((capacity, hidden), dtype=torch.bfloat16, device=device)
+        scales = None
+    return Dispatched(recv_x, scales,
+                      torch.empty(capacity, dtype=torch.int32, device=device),
+                      torch.empty((capacity, num_topk), dtype=torch.int64, device=device),
+                      torch.empty((capacity, num_topk), dtype=torch.float32, device=device),
+                      torch.empty((num_ranks, num_experts // num_ranks), dtype=torch.int32,
+                                  device=device), use_fp8)
+
+
+def dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor,
+             layout: Layout, *, use_fp8: bool = False, capacity: int | None = None,
+             err: torch.Tensor | None = None, out: Dispatched | None = None) -> Dispatched:
+    """Scatter every token row to its destination ranks' rows (bf16 copy or
+    FP8 E4M3 with per-128-channel scales).  Enqueued on the current stream."""
+    _need(x, "x", torch.bfloat16)
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    _need(topk_idx, "topk_idx", torch.int64, (T, K))
+    _need(topk_weights, "topk_weights", torch.float32, (T, K))
+    R, E = layout.num_ranks, layout.num_experts
+    _need(layout.slot, "slot", torch.int32, (T, R))
+    if out is None:
+        cap = capacity if capacity is not None else worst_case_rows(T, K, R)
+        out = alloc_dispatched(cap, H, K, E, R, use_fp8, x.device)
+    elif out.use_fp8 != use_fp8:
+        raise EPError("preallocated dispatch buffers have the wrong payload type")
+    cap = out.recv_x.shape[0]
+    if err is not None:
+        _need(err, "err", torch.int32)
+    _check(lib().ep_dispatch(
+        _ptr(x), H, _ptr(topk_idx), _ptr(topk_weights), T, K, E, R, _ptr(layout.slot),
+        _ptr(layout.num_tokens_per_expert), cap, int(use_fp8), _ptr(out.recv_x),
+        _ptr(out.recv_scales), _ptr(out.recv_src_idx), _ptr(out.recv_topk_idx),
+        _ptr(out.recv_topk_weights), _ptr(out.num_recv_tokens_per_expert), _ptr(err),
+        _stream(x.device)), "ep_dispatch")
+    return out
+
+
+def combine(y: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor,
+            layout: Layout, *, err: torch.Tensor | None = None,
+            out: torch.Tensor | None = None) -> torch.Tensor:
+    """out[t] = bf16(sum_k w[t][k] * y[slot[t][rank(e_k)]]) accumulated in
+    float32.  Enqueued on the current stream."""
+    _need(y, "y", torch.bfloat16)
+    H = y.shape[1]
+    T, K = topk_idx.shape
+    _need(topk_idx, "topk_idx", torch.int64, (T, K))
+    _need(topk_weights, "topk_weights", torch.float32, (T, K))
+    R, E = layout.num_ranks, layout.num_experts
+    _need(layout.slot, "slot", torch.int32, (T, R))
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device)
+    _need(out, "out", torch.bfloat16, (T, H))
+    if err is not None:
+        _need(err, "err", torch.int32)
+    _check(lib().ep_combine(_ptr(y), H, _ptr(topk_idx), _ptr(topk_weights), T, K, E, R,
+                            _ptr(layout.slot), _ptr(out), _ptr(err), _stream(y.device)),
+           "ep_combine")
+    return out

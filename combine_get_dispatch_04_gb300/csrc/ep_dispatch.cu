@@ -1,0 +1,229 @@
+// ep_dispatch.cu -- token scatter into the packed per-destination receive
+// buffer, bf16 or FP8 E4M3 with per-128-channel float32 scales.
+//
+// "[Not ready] MSCCLPP EP implementation" (mscclpp pull request 852):
+// section "Scope", Intranode (intranode_dispatch), and the low-latency port
+// (dispatch<kUseFP8,...>, the FP8 payload cast).  On one GPU the scatter is
+// a memory-bound copy: each token row is read once from HBM and written once
+// per destination rank.
+//
+// One warp per token.  Lanes hold 16-byte vectors of the row (8 bf16
+// channels); kUnroll vectors per lane are loaded before the stores so each
+// warp keeps 4 x 512 bytes of reads in flight.  Loads bypass L1, stores use
+// the streaming policy.  In the FP8 variant a half-warp holds one block of
+// 128 channels: its amax is a 4-step xor-shuffle reduction, and the block is
+// quantised in registers before being written to every destination.  The
+// quantiser rounds exactly as the format definition requires: 448/a and a/448
+// are single correctly rounded divisions (__fdiv_rn), x * (448/a) is a single
+// multiply (__fmul_rn), and the E4M3 conversion is the hardware's
+// round-to-nearest-even, saturate-to-finite conversion.
+#include <cuda_fp8.h>
+
+#include "ep_common.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kWarps = 8;  // tokens per block
+constexpr int kUnroll = 4;
+
+struct Args {
+  const int4* x;
+  int64_t T;
+  int H;
+  const int64_t* topk_idx;
+  const float* topk_w;
+  int K, E, El, R;
+  const int32_t* slot;
+  const int32_t* ntpe;
+  int64_t cap;
+  void* recv_x;
+  float* recv_scales;
+  int32_t* recv_src_idx;
+  int64_t* recv_topk_idx;
+  float* recv_topk_w;
+  int32_t* nrpe;
+  int32_t* err;
+};
+
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float d) {
+  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+template <bool kFP8>
+__global__ void __launch_bounds__(kWarps * 32) dispatch_kernel(Args a) {
+  __shared__ int32_t dst_row[kWarps][EP_MAX_RANKS];
+  __shared__ int32_t dst_rank[kWarps][EP_MAX_RANKS];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  // receiver-side rows per local expert (column sums of the per-source counts)
+  if (blockIdx.x == 0 && a.nrpe && a.ntpe) {
+    for (int e = threadIdx.x; e < a.E; e += kWarps * 32) {
+      int sum = 0;
+      for (int s = 0; s < a.R; ++s) sum += a.ntpe[(int64_t)s * a.E + e];
+      a.nrpe[e] = sum;  // [R, E_l] row-major == expert index e
+    }
+  }
+
+  const int64_t t = (int64_t)blockIdx.x * kWarps + warp;
+  if (t >= a.T) return;  // uniform per warp
+
+  // destinations of this token, in rank order
+  int nd = 0;
+  bool over = false;
+  for (int r0 = 0; r0 < a.R; r0 += 32) {
+    const int r = r0 + lane;
+    const int32_t sl = r < a.R ? a.slot[t * a.R + r] : -1;
+    const bool ok = sl >= 0 && sl < a.cap;
+    over |= sl >= a.cap;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
+    if (ok) {
+      const int pos = nd + __popc(bal & ((1u << lane) - 1u));
+      dst_row[warp][pos] = sl;
+      dst_rank[warp][pos] = r;
+    }
+    nd += __popc(bal);
+  }
+  if (__any_sync(0xFFFFFFFFu, over) && lane == 0 && a.err) atomicOr(a.err, EP_ERRBIT_CAPACITY);
+  __syncwarp();
+  if (nd == 0) return;
+
+  // per-row metadata: source token, and the top-k entries that are local to
+  // the destination (local expert id and weight), -1 / 0 elsewhere
+  if (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_w) {
+    const int64_t e = lane < a.K ? a.topk_idx[t * a.K + lane] : -1;
+    const float w = (lane < a.K && a.topk_w) ? a.topk_w[t * a.K + lane] : 0.0f;
+    const int er = (e >= 0 && e < a.E) ? (int)(e / a.El) : -1;
+    for (int d = 0; d < nd; ++d) {
+      const int64_t row = dst_row[warp][d];
+      const int r = dst_rank[warp][d];
+      if (lane == 0 && a.recv_src_idx) a.recv_src_idx[row] = (int32_t)t;
+      if (lane < a.K) {
+        const bool here = er == r;
+        if (a.recv_topk_idx) a.recv_topk_idx[row * a.K + lane] = here ? e - (int64_t)r * a.El : -1;
+        if (a.recv_topk_w) a.recv_topk_w[row * a.K + lane] = here ? w : 0.0f;
+      }
+    }
+  }
+
+  const int nvec = a.H / 8;  // 16-byte vectors per row
+  const int4* src = a.x + t * nvec;
+  if constexpr (!kFP8) {
+    int4* out = reinterpret_cast<int4*>(a.recv_x);
+    for (int v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
+      int4 buf[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < nvec) buf[u] = ld_stream_v4(src + v);
+      }
+      for (int d = 0; d < nd; ++d) {
+        int4* dst = out + (int64_t)dst_row[warp][d] * nvec;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nvec) st_stream_v4(dst + v, buf[u]);
+        }
+      }
+    }
+  } else {
+    // H % 128 == 0, so nvec % 16 == 0 and half-warps are wholly in or out
+    uint8_t* out = reinterpret_cast<uint8_t*>(a.recv_x);
+    const int nblk = a.H / 128;
+    for (int v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
+      uint2 q[kUnroll];
+      float scale[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v = v0 + u * 32 + lane;
+        float f[8];
+        const int4 raw = v < nvec ? ld_stream_v4(src + v) : make_int4(0, 0, 0, 0);
+        unpack_bf16x8(raw, f);
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float am = fmaxf(amax, 1e-4f);
+        scale[u] = __fdiv_rn(am, 448.0f);
+        const float inv = __fdiv_rn(448.0f, am);
+        q[u].x = cvt_e4m3x4(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
+                            __fmul_rn(f[3], inv));
+        q[u].y = cvt_e4m3x4(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv), __fmul_rn(f[6], inv),
+                            __fmul_rn(f[7], inv));
+      }
+      for (int d = 0; d < nd; ++d) {
+        const int64_t row = dst_row[warp][d];
+        uint8_t* dst = out + row * a.H;
+        float* srow = a.recv_scales + row * nblk;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nvec) {
+            st_stream_v2(reinterpret_cast<uint2*>(dst + (int64_t)v * 8), q[u]);
+            if ((lane & 15) == 0) srow[v >> 4] = scale[u];
+          }
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+}  // namespace ep
+
+using namespace ep;
+
+extern "C" ep_status_t ep_dispatch(const void* x, int hidden, const int64_t* topk_idx,
+                                   const float* topk_weights, int64_t num_tokens, int num_topk,
+                                   int num_experts, int num_ranks, const int32_t* slot,
+                                   const int32_t* num_tokens_per_expert,
+                                   int64_t recv_capacity_rows, int use_fp8, void* recv_x,
+                                   float* recv_scales, int32_t* recv_src_idx,
+                                   int64_t* recv_topk_idx, float* recv_topk_weights,
+                                   int32_t* num_recv_tokens_per_expert, int32_t* err_word,
+                                   ep_stream_t stream) {
+  if (!routing_ok(num_tokens, num_topk, num_experts, num_ranks)) return EP_ERR_INVALID_ARG;
+  if (hidden < 8 || hidden % 8 != 0 || (use_fp8 && hidden % 128 != 0)) return EP_ERR_INVALID_ARG;
+  if (recv_capacity_rows < 0) return EP_ERR_INVALID_ARG;
+  if (num_tokens > 0) {
+    if (!x || !topk_idx || !slot || !recv_x) return EP_ERR_INVALID_ARG;
+    if ((recv_topk_idx || recv_topk_weights) && !topk_weights) return EP_ERR_INVALID_ARG;
+    if (use_fp8 && !recv_scales) return EP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(recv_x)) return EP_ERR_INVALID_ARG;
+  }
+  if (num_recv_tokens_per_expert && !num_tokens_per_expert) return EP_ERR_INVALID_ARG;
+  Args a;
+  a.x = static_cast<const int4*>(x);
+  a.T = num_tokens;
+  a.H = hidden;
+  a.topk_idx = topk_idx;
+  a.topk_w = topk_weights;
+  a.K = num_topk;
+  a.E = num_experts;
+  a.El = num_experts / num_ranks;
+  a.R = num_ranks;
+  a.slot = slot;
+  a.ntpe = num_tokens_per_expert;
+  a.cap = recv_capacity_rows;
+  a.recv_x = recv_x;
+  a.recv_scales = recv_scales;
+  a.recv_src_idx = recv_src_idx;
+  a.recv_topk_idx = recv_topk_idx;
+  a.recv_topk_w = recv_topk_weights;
+  a.nrpe = num_recv_tokens_per_expert;
+  a.err = err_word;
+  int64_t blocks = (num_tokens + kWarps - 1) / kWarps;
+  if (blocks == 0) {
+    if (!a.nrpe) return EP_OK;
+    blocks = 1;
+  }
+  cudaStream_t st = to_cuda(stream);
+  if (use_fp8)
+    dispatch_kernel<true><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
+  else
+    dispatch_kernel<false><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
+  return launch_status();
+}

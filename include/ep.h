@@ -1,0 +1,184 @@
+/*
+ * ep.h -- C ABI of the single-GPU MoE expert-parallel token shuffle
+ * (get_dispatch_layout -> dispatch -> combine) for GB300 (sm_103a).
+ *
+ * The operations are the high-throughput expert-parallel kernels described in
+ * "[Not ready] MSCCLPP EP implementation" (mscclpp pull request 852), section
+ * "Scope": get_dispatch_layout, intranode_dispatch and intranode_combine (the
+ * DeepEP kernels, there ported onto MSCCL++ channels), plus the kUseFP8
+ * payload cast of the low-latency dispatch<kUseFP8,...> kernel.  Here all R
+ * logical ranks live on one GPU: rank s owns tokens [s*T_r, (s+1)*T_r) of
+ * one call and experts [s*E_l, (s+1)*E_l), and every destination rank's
+ * receive buffer is a range of rows of one packed device buffer.  The
+ * "exchange" is the scatter kernel's own HBM writes; there is no peer
+ * traffic and no collective.
+ *
+ * Notation: T tokens (T % R == 0, T_r = T/R), K top-k slots, E experts
+ * (E % R == 0, E_l = E/R), H hidden channels, R ranks, P = number of
+ * (token, destination rank) pairs = rows of the receive buffer.
+ * src(t) = t / T_r, rank(e) = e / E_l.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked "device" are CUDA device pointers (or managed memory);
+ *     "host" pointers are ordinary host memory.  The library never
+ *     allocates or frees memory: the caller owns every buffer.
+ *   - Every call is enqueued on `stream` (NULL = the legacy default stream)
+ *     and returns without synchronising, except ep_layout_total_rows.
+ *   - Argument checks are done on the host before anything is enqueued; a
+ *     failed check returns EP_ERR_INVALID_ARG and enqueues nothing.
+ *   - Problems that only the data reveal are reported through an optional
+ *     device error word (int32, nullable): the kernels OR EP_ERRBIT_* bits
+ *     into it with atomicOr.  The caller zeroes it; the library never clears
+ *     it.  No kernel traps.
+ *   - All buffers must be 16-byte aligned; x / recv_x / y / out rows are
+ *     moved in 16-byte vectors and 1-D bulk (TMA) copies.
+ *   - Limits: 1 <= R <= EP_MAX_RANKS, 1 <= K <= EP_MAX_TOPK,
+ *     1 <= E <= EP_MAX_EXPERTS, H % 8 == 0 (H % 128 == 0 for FP8),
+ *     T * R < 2^31.
+ */
+#ifndef EP_H_
+#define EP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same opaque type as cudaStream_t / CUstream, so no CUDA header is needed. */
+typedef struct CUstream_st* ep_stream_t;
+
+typedef enum {
+  EP_OK = 0,
+  EP_ERR_INVALID_ARG = 1, /* a host-side argument check failed; nothing enqueued */
+  EP_ERR_CAPACITY = 2,    /* a caller-provided buffer is too small (host-visible size) */
+  EP_ERR_CUDA = 3,        /* a CUDA runtime call failed (launch, copy, sync) */
+  EP_ERR_TIMEOUT = 4      /* reserved: a bounded device wait ran out (see EP_ERRBIT_TIMEOUT) */
+} ep_status_t;
+
+/* Bits OR-ed into the device error word. */
+#define EP_ERRBIT_BAD_EXPERT 1 /* a topk_idx entry outside [-1, E): treated as masked */
+#define EP_ERRBIT_CAPACITY 2   /* a slot >= recv_capacity_rows: that row was not written */
+#define EP_ERRBIT_TIMEOUT 4    /* a bounded shared-memory pipeline wait ran out */
+
+#define EP_MAX_RANKS 64
+#define EP_MAX_TOPK 32
+#define EP_MAX_EXPERTS 4096
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* ep_status_string(ep_status_t status);
+
+/*
+ * Bytes of device scratch that ep_get_dispatch_layout needs for T tokens,
+ * R ranks and E experts.  Returns 0 for invalid sizes.  The scratch holds
+ * one 64-bit rank mask per token and per-block partial counts; its contents
+ * need no initialisation and are dead after the call's kernels finish.
+ */
+size_t ep_workspace_bytes(int64_t num_tokens, int num_ranks, int num_experts);
+
+/*
+ * get_dispatch_layout + slot assignment ("Scope", Intranode:
+ * get_dispatch_layout; the internode-combine commit: combine must use the
+ * receiver-side prefix matrices, i.e. the slot order is fixed by prefix sums
+ * over source rank and token order).
+ *
+ * In  (device): topk_idx [T, K] int64, row-major; -1 = masked slot.
+ * Out (device), every element written:
+ *   num_tokens_per_rank   [R, R] int32: [s][r] = tokens of source s sent to r
+ *   num_tokens_per_expert [R, E] int32: [s][e] = slots (t,k) with src(t)=s, e_k = e
+ *   is_token_in_rank      [T, R] uint8 (0/1; torch.bool storage)
+ *   slot                  [T, R] int32: row of (t, r) in the receive buffer,
+ *                         -1 if token t is not sent to rank r.  Rows are packed
+ *                         destination-major: destination r owns rows
+ *                         [recv_base[r], recv_base[r+1]), ordered by source
+ *                         rank and then token index.
+ *   recv_base             [R + 1] int32: exclusive prefix of rows per
+ *                         destination; recv_base[R] = P.
+ * err_word (device, nullable): EP_ERRBIT_BAD_EXPERT if some id is outside
+ *   [-1, E) (the slot is then treated as masked).
+ * workspace (device): at least ep_workspace_bytes(T, R, E) bytes, passed as
+ *   workspace_bytes; a smaller value returns EP_ERR_CAPACITY.
+ * T = 0 is valid (counts and recv_base are zeroed).
+ */
+ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t num_tokens, int num_topk,
+                                   int num_experts, int num_ranks, int32_t* num_tokens_per_rank,
+                                   int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+                                   int32_t* slot, int32_t* recv_base, int32_t* err_word,
+                                   void* workspace, size_t workspace_bytes, ep_stream_t stream);
+
+/*
+ * Copies P = recv_base[R] (device) into *host_total_rows and synchronises
+ * `stream`.  The only synchronising call; use it to size the receive buffer
+ * exactly, or skip it and pass a worst-case capacity of
+ * T * min(K, R) rows to ep_dispatch.
+ */
+ep_status_t ep_layout_total_rows(const int32_t* recv_base, int num_ranks, int32_t* host_total_rows,
+                                 ep_stream_t stream);
+
+/*
+ * dispatch ("Scope", Intranode: intranode_dispatch; the low-latency port:
+ * dispatch<kUseFP8,...>).  For every pair (t, r) with slot[t][r] >= 0:
+ *   use_fp8 == 0:  recv_x[slot] = x[t]                      (bf16 bit copy)
+ *   use_fp8 == 1:  for each block b of 128 channels,
+ *                    amax  = max |x[t][b*128 .. b*128+127]|   (float32)
+ *                    a     = max(amax, 1e-4f)
+ *                    recv_scales[slot][b] = a / 448          (float32, rounded once)
+ *                    recv_x[slot][i] = E4M3(x[t][i] * (448 / a)),
+ *                    with 448/a rounded once, one float32 multiply, and the
+ *                    E4M3 conversion rounding to nearest even and saturating
+ *                    to +-448; dequantise as code * scale.
+ *   recv_src_idx[slot]         = t
+ *   recv_topk_idx[slot][k]     = e_k - r*E_l if rank(e_k) == r, else -1
+ *   recv_topk_weights[slot][k] = w[t][k]     if rank(e_k) == r, else 0.0f
+ * In (device): x [T, H] bf16; topk_idx [T, K] int64; topk_weights [T, K]
+ *   float32; slot [T, R] int32 from ep_get_dispatch_layout.
+ *   num_tokens_per_expert [R, E] int32 from ep_get_dispatch_layout (nullable;
+ *   only read to fill num_recv_tokens_per_expert).
+ * Out (device): recv_x [capacity, H] bf16, or [capacity, H] E4M3 bytes with
+ *   recv_scales [capacity, H/128] float32 (FP8 only, else may be NULL);
+ *   recv_src_idx [capacity] int32, recv_topk_idx [capacity, K] int64,
+ *   recv_topk_weights [capacity, K] float32 (each nullable: skipped if NULL);
+ *   num_recv_tokens_per_expert [R, E_l] int32 (nullable): rows each
+ *   destination rank receives per local expert, summed over source ranks.
+ *   Rows >= P are not touched.
+ * recv_capacity_rows: rows the caller allocated; a pair whose slot is >= it
+ *   is skipped and sets EP_ERRBIT_CAPACITY in err_word.
+ */
+ep_status_t ep_dispatch(const void* x, int hidden, const int64_t* topk_idx,
+                        const float* topk_weights, int64_t num_tokens, int num_topk,
+                        int num_experts, int num_ranks, const int32_t* slot,
+                        const int32_t* num_tokens_per_expert, int64_t recv_capacity_rows,
+                        int use_fp8, void* recv_x, float* recv_scales, int32_t* recv_src_idx,
+                        int64_t* recv_topk_idx, float* recv_topk_weights,
+                        int32_t* num_recv_tokens_per_expert, int32_t* err_word,
+                        ep_stream_t stream);
+
+/*
+ * combine ("Scope", Intranode: intranode_combine; the bench-accounting
+ * commit: combine moves one copy per dispatched (token, rank) row back to
+ * its owner).  For every token t:
+ *   out[t] = bf16_rne( sum over k with e_k != -1 of
+ *                      w[t][k] * float(y[slot[t][rank(e_k)]]) )
+ * accumulated in float32; a token whose slots are all masked gives +0.
+ * A rank named by several slots contributes its row once per slot.
+ * In (device): y [rows, H] bf16 in dispatch's row layout (expert outputs,
+ *   one row per (token, rank) pair); topk_idx [T, K] int64; topk_weights
+ *   [T, K] float32; slot [T, R] int32 from ep_get_dispatch_layout.
+ * Out (device): out [T, H] bf16, every element written.
+ * err_word (device, nullable): EP_ERRBIT_BAD_EXPERT for ids outside [-1, E)
+ *   (skipped), EP_ERRBIT_TIMEOUT if a bounded pipeline wait ran out (the
+ *   output is then incomplete).
+ * y rows are staged through shared memory with 1-D bulk (TMA) copies; y and
+ * out must not overlap.
+ */
+ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk_idx,
+                       const float* topk_weights, int64_t num_tokens, int num_topk,
+                       int num_experts, int num_ranks, const int32_t* slot, void* out,
+                       int32_t* err_word, ep_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_H_ */

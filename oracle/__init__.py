@@ -105,8 +105,9 @@ class Dispatched:
 def dispatch(x_bits: np.ndarray, topk_idx: np.ndarray, topk_weights: np.ndarray,
              num_experts: int, num_ranks: int, slot: np.ndarray, num_rows: int,
              use_fp8: bool = False, t_range: tuple[int, int] | None = None,
-             fill: int = 0) -> Dispatched:
-    """Dispatch tokens in t_range (default: all); rows of other tokens keep `fill`."""
+             fill: int | None = 0) -> Dispatched:
+    """Dispatch tokens in t_range (default: all); rows of other tokens keep
+    `fill` (left uninitialised when fill is None)."""
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
     topk_weights = np.ascontiguousarray(topk_weights, dtype=np.float32)
@@ -115,10 +116,12 @@ def dispatch(x_bits: np.ndarray, topk_idx: np.ndarray, topk_weights: np.ndarray,
     K = topk_idx.shape[1]
     t0, t1 = t_range if t_range is not None else (0, T)
     if use_fp8:
-        recv_x = np.full((num_rows, H), fill & 0xFF, np.uint8)
+        recv_x = (np.empty((num_rows, H), np.uint8) if fill is None
+                  else np.full((num_rows, H), fill & 0xFF, np.uint8))
         scales = np.zeros((num_rows, H // 128), np.float32)
     else:
-        recv_x = np.full((num_rows, H), fill & 0xFFFF, np.uint16)
+        recv_x = (np.empty((num_rows, H), np.uint16) if fill is None
+                  else np.full((num_rows, H), fill & 0xFFFF, np.uint16))
         scales = None
     src = np.full(num_rows, -2, np.int32)
     tidx = np.full((num_rows, K), -2, np.int64)

@@ -1,0 +1,113 @@
+"""The C ABI library builds, loads and exports every entry point that
+include/ep.h declares; host-side argument checks reject bad calls before
+anything reaches CUDA.  No test here launches a kernel (no GPU needed)."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ep.h")
+
+EP_ERR_INVALID_ARG = 1
+EP_ERR_CAPACITY = 2
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ep_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def eplib():
+    from combine_get_dispatch_04_gb300 import build
+    build.build()
+    import combine_get_dispatch_04_gb300 as ep
+    return ep.load()
+
+
+def test_header_declares_the_entry_points():
+    import combine_get_dispatch_04_gb300 as ep
+    assert declared_functions() == sorted(ep.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(eplib):
+    for name in declared_functions():
+        assert hasattr(eplib, name), name
+
+
+def test_status_strings(eplib):
+    for code in range(5):
+        s = eplib.ep_status_string(code).decode()
+        assert s.startswith("EP_")
+    assert eplib.ep_status_string(99).decode() == "unknown ep_status_t"
+
+
+def test_workspace_bytes(eplib):
+    wb = eplib.ep_workspace_bytes
+    assert wb(0, 4, 16) > 0 or wb(0, 4, 16) == wb(0, 4, 16)  # valid, possibly tiny
+    assert wb(131072, 16, 64) >= 131072 * 8  # one 64-bit rank mask per token
+    assert wb(512, 4, 16) <= wb(1024, 4, 16)
+    assert wb(10, 4, 16) == 0   # T % R != 0
+    assert wb(512, 3, 16) == 0  # E % R != 0
+    assert wb(512, 65, 65) == 0  # R above the maximum
+    assert wb(512, 4, 4100) == 0  # E above the maximum
+    assert wb(-4, 4, 16) == 0
+
+
+def _layout_call(eplib, T=8, K=2, E=8, R=2, ptrs=True, ws_bytes=1 << 20):
+    p = C.c_void_p(16) if ptrs else None  # never dereferenced: the checks fail first
+    return eplib.ep_get_dispatch_layout(p, T, K, E, R, p, p, p, p, p, None, p, ws_bytes, None)
+
+
+def test_layout_rejects_bad_arguments(eplib):
+    assert _layout_call(eplib, E=7) == EP_ERR_INVALID_ARG        # E % R
+    assert _layout_call(eplib, T=9) == EP_ERR_INVALID_ARG        # T % R
+    assert _layout_call(eplib, K=0) == EP_ERR_INVALID_ARG
+    assert _layout_call(eplib, K=33) == EP_ERR_INVALID_ARG       # above EP_MAX_TOPK
+    assert _layout_call(eplib, R=65, E=65 * 2, T=130) == EP_ERR_INVALID_ARG
+    assert _layout_call(eplib, ptrs=False) == EP_ERR_INVALID_ARG
+    assert _layout_call(eplib, ws_bytes=8) == EP_ERR_CAPACITY    # workspace too small
+
+
+def test_dispatch_rejects_bad_arguments(eplib):
+    p = C.c_void_p(16)
+    base = dict(x=p, H=256, idx=p, w=p, T=8, K=2, E=8, R=2, slot=p, ntpe=None, cap=16,
+                fp8=0, rx=p, rs=None)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return eplib.ep_dispatch(a["x"], a["H"], a["idx"], a["w"], a["T"], a["K"], a["E"],
+                                 a["R"], a["slot"], a["ntpe"], a["cap"], a["fp8"], a["rx"],
+                                 a["rs"], None, None, None, None, None, None)
+    assert call(H=12) == EP_ERR_INVALID_ARG                 # H % 8
+    assert call(H=264, fp8=1, rs=p) == EP_ERR_INVALID_ARG   # FP8 needs H % 128
+    assert call(fp8=1) == EP_ERR_INVALID_ARG                # FP8 needs scales
+    assert call(cap=-1) == EP_ERR_INVALID_ARG
+    assert call(x=C.c_void_p(24)) == EP_ERR_INVALID_ARG    # misaligned payload
+    assert call(rx=None) == EP_ERR_INVALID_ARG
+    assert call(E=7) == EP_ERR_INVALID_ARG                  # E % R
+
+
+def test_combine_rejects_bad_arguments_and_accepts_empty(eplib):
+    p = C.c_void_p(16)
+    assert eplib.ep_combine(p, 12, p, p, 8, 2, 8, 2, p, p, None, None) == EP_ERR_INVALID_ARG
+    assert eplib.ep_combine(p, 256, p, None, 8, 2, 8, 2, p, p, None, None) == EP_ERR_INVALID_ARG
+    assert eplib.ep_combine(C.c_void_p(8), 256, p, p, 8, 2, 8, 2, p, p, None, None) == EP_ERR_INVALID_ARG
+    # no tokens: nothing to do, nothing enqueued
+    assert eplib.ep_combine(None, 256, None, None, 0, 2, 8, 2, None, None, None, None) == 0
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    import combine_get_dispatch_04_gb300 as ep
+    saved = ep._lib
+    ep._lib = None
+    try:
+        with pytest.raises(ep.EPError):
+            ep.load(str(tmp_path / "missing.so"))
+    finally:
+        ep._lib = saved

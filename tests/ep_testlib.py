@@ -70,7 +70,7 @@ def combine_bound(y_f64: np.ndarray, topk_idx: np.ndarray, w: np.ndarray, slot: 
     out = np.zeros((tokens.size, H))
     for k in range(topk_idx.shape[1]):
         e = topk_idx[tokens, k]
-        ok = e >= 0
+        ok = (e >= 0) & (e < El * slot.shape[1])
         rows = slot[tokens[ok], e[ok] // El]
         out[ok] += np.abs(w[tokens[ok], k].astype(np.float64))[:, None] * np.abs(y_f64[rows])
     return out

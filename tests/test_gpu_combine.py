@@ -64,8 +64,8 @@ def test_combine_one_hot_weights_bit_exact(ep):
 
 @pytest.mark.parametrize("cfg", small_configs(), ids=lambda c: c.name)
 def test_round_trip_identity_experts_small(ep, cfg):
-    """combine(dispatch(x)) == x bit for bit with identity experts and weights
-    renormalised to sum to one ("combine diff=0"); all-masked tokens give 0."""
+    """combine(dispatch(x)) == x with identity experts and weights renormalised
+    to sum to one ("combine diff=0"), compared as values; all-masked tokens give 0."""
     c = make_case(cfg)
     idx, _, x = device_inputs(c)
     w_np = renormalised(c)
@@ -75,7 +75,9 @@ def test_round_trip_identity_experts_small(ep, cfg):
     out = ep.combine(d.recv_x, idx, w, L)
     got = bits_of(out)
     live = (c.topk_idx >= 0).any(axis=1)
-    np.testing.assert_array_equal(got[live], c.x_bits[live])
+    # equal as values (a -0.0 in x returns as +0.0); masked tokens give +0
+    np.testing.assert_array_equal(oracle.bf16_to_double(got[live]),
+                                  oracle.bf16_to_double(c.x_bits[live]))
     assert (got[~live] == 0).all()
 
 
@@ -115,7 +117,7 @@ def test_combine_full_size(ep, name):
     (identity experts; for FP8 dispatch, random bf16 expert outputs, since
     combine is bf16 in / bf16 out).  Sampled token ranges are compared with
     the oracle within the tolerance; with weights renormalised over the live
-    slots every token must come back bit for bit (bf16 workloads)."""
+    slots every token must come back exactly (as values; bf16 workloads)."""
     cfg = CONFIGS[name]
     c, want_layout = full_case(name)
     idx, w, x = device_inputs(c)
@@ -147,5 +149,15 @@ def test_combine_full_size(ep, name):
         wn = torch.from_numpy(renormalised(c)).cuda()
         out2 = ep.combine(d.recv_x, idx, wn, L)
         live = torch.from_numpy((c.topk_idx >= 0).any(axis=1)).cuda()
-        assert torch.equal(out2[live].view(torch.int16), x[live].view(torch.int16))
+        # values, not bits: a -0.0 in x comes back as +0.0 (0 + w * -0 = +0)
+        diff = (out2.float() != x.float()).any(dim=1) & live
+        if bool(diff.any()):
+            bad = torch.nonzero(diff).flatten().cpu().numpy()
+            t = int(bad[0])
+            rows = [int(s) for s in slot[t] if s >= 0]
+            same = [bool(torch.equal(d.recv_x[r].view(torch.int16), x[t].view(torch.int16)))
+                    for r in rows]
+            ndiff = int((out2[t].float() != x[t].float()).sum())
+            raise AssertionError(f"{bad.size} tokens differ (first {bad[:8].tolist()}); token {t}: "
+                                 f"rows {rows} equal x: {same}; {ndiff} channels differ")
         assert not out2[~live].view(torch.int16).any()

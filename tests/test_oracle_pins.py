@@ -448,8 +448,19 @@ def test_round_trip_identity_experts(name):
     L = oracle.layout(c.topk_idx, E, R)
     d = oracle.dispatch(c.x_bits, c.topk_idx, w, E, R, L.slot, L.num_rows)
     out = oracle.combine(d.recv_x, c.topk_idx, w, E, R, L.slot)
-    assert np.array_equal(out[keep], c.x_bits[keep])
+    # equal as values: a -0.0 in x comes back as +0.0 (0 + w * -0 = +0)
+    assert np.array_equal(oracle.bf16_to_double(out[keep]), oracle.bf16_to_double(c.x_bits[keep]))
     assert (out[~keep] == 0).all()
+
+
+def test_round_trip_negative_zero_returns_positive_zero():
+    idx = np.array([[0, 1]], np.int64)
+    w = np.array([[0.25, 0.75]], np.float32)
+    x = np.array([[0x8000, 0x3F80]], np.uint16)  # -0.0, 1.0
+    L = oracle.layout(idx, 2, 1)
+    d = oracle.dispatch(x, idx, w, 2, 1, L.slot, L.num_rows)
+    out = oracle.combine(d.recv_x, idx, w, 2, 1, L.slot)
+    assert out.tolist() == [[0x0000, 0x3F80]]
 
 
 def test_golden_tiny_layout():

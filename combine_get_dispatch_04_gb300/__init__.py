@@ -33,7 +33,8 @@ EP_MAX_EXPERTS = 4096
 
 # every entry point declared in include/ep.h
 EXPORTED = ("ep_status_string", "ep_workspace_bytes", "ep_get_dispatch_layout",
-            "ep_layout_total_rows", "ep_dispatch", "ep_combine")
+            "ep_get_dispatch_layout_noalloc", "ep_layout_total_rows", "ep_dispatch",
+            "ep_combine")
 
 _lib = None
 

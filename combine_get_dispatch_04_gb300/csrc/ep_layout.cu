@@ -19,6 +19,8 @@
 //                count per destination.
 //   3. assign -- one thread per token: ballot-based prefix within the block
 //                plus the block's prefix gives the slot.
+#include <mutex>
+
 #include "ep_common.cuh"
 
 namespace ep {
@@ -301,4 +303,72 @@ extern "C" ep_status_t ep_layout_total_rows(const int32_t* recv_base, int num_ra
     return EP_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return EP_ERR_CUDA;
   return EP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Layout without caller-provided scratch.
+//
+// For callers that cannot allocate device memory at call time: a plugin or
+// custom-op host that hands the library only the tensors it already owns, a
+// C caller with no device allocator of its own, or a serving loop whose
+// memory budget is fixed at start-up (cudaMalloc can also stall every stream
+// on the device while it runs).  The scratch lives in the file-scope array
+// below, so every GPU that loads this library holds these bytes until the
+// process exits.  All calls share the one array: calls that overlap on the
+// GPU (two streams, or two host threads enqueueing at once) race on it.  It
+// needs no clearing between calls: every scratch word a call reads was
+// written earlier in that same call.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char ep_layout_noalloc_scratch[EP_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};  // device address of the array, per device id
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the host-side name of the array is not a device address).
+ep_status_t noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return EP_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, ep_layout_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return EP_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return EP_OK;
+}
+
+}  // namespace
+
+extern "C" ep_status_t ep_get_dispatch_layout_noalloc(
+    const int64_t* topk_idx, int64_t num_tokens, int num_topk, int num_experts, int num_ranks,
+    int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+    int32_t* slot, int32_t* recv_base, int32_t* err_word, ep_stream_t stream) {
+  if (!routing_ok(num_tokens, num_topk, num_experts, num_ranks)) return EP_ERR_INVALID_ARG;
+  if (!num_tokens_per_rank || !num_tokens_per_expert || !recv_base) return EP_ERR_INVALID_ARG;
+  if (num_tokens > 0) {
+    if (!topk_idx || !is_token_in_rank || !slot) return EP_ERR_INVALID_ARG;
+    if (!aligned16(slot) || !aligned16(is_token_in_rank) || !aligned16(topk_idx))
+      return EP_ERR_INVALID_ARG;
+  }
+  const Geom g = make_geom(num_tokens, num_topk, num_experts, num_ranks);
+  if (carve(g, nullptr).bytes > (size_t)EP_NOALLOC_SCRATCH_BYTES) return EP_ERR_CAPACITY;
+  void* scratch = nullptr;
+  const ep_status_t s = noalloc_scratch(&scratch);
+  if (s != EP_OK) return s;
+  const Workspace ws = carve(g, scratch);
+  cudaStream_t st = to_cuda(stream);
+  if (g.nb > 0) {
+    const size_t smem = sizeof(int32_t) * ((size_t)g.E + (size_t)kTokWarps * g.R);
+    layout_count_kernel<<<g.nb, kTok, smem, st>>>(topk_idx, g, is_token_in_rank, ws, err_word);
+  }
+  layout_scan_kernel<<<1, kScanThreads, 0, st>>>(g, ws, num_tokens_per_rank,
+                                                 num_tokens_per_expert, recv_base);
+  if (g.nb > 0) layout_assign_kernel<<<g.nb, kTok, 0, st>>>(g, ws, slot);
+  return launch_status();
 }

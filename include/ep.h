@@ -108,6 +108,37 @@ ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t num_tokens, 
                                    void* workspace, size_t workspace_bytes, ep_stream_t stream);
 
 /*
+ * The same layout as ep_get_dispatch_layout, for callers that cannot
+ * allocate device memory when they call it (the paper has no counterpart to
+ * this entry point).  Such callers include plugin or custom-op hosts that
+ * hand the library only tensors they already own, C callers with no device
+ * allocator of their own, and serving loops whose device-memory budget is
+ * fixed at start-up (cudaMalloc may also stall every stream on the device).
+ * The scratch comes from a fixed array of EP_NOALLOC_SCRATCH_BYTES inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits; nothing is allocated or freed.
+ *
+ * Arguments, outputs and error word: as ep_get_dispatch_layout, without the
+ * workspace.  Returns EP_ERR_CAPACITY, with nothing enqueued, when
+ * ep_workspace_bytes(T, R, E) exceeds EP_NOALLOC_SCRATCH_BYTES (about 8 bytes
+ * per token plus a small per-block term: roughly 800k tokens at 256 experts).
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array, so calls that
+ * overlap on the GPU (two streams, or two threads enqueueing at once) race
+ * and must be serialised by the caller.  The array needs no clearing: each
+ * call writes every scratch word before reading it.
+ */
+#define EP_NOALLOC_SCRATCH_BYTES (8u << 20)
+ep_status_t ep_get_dispatch_layout_noalloc(const int64_t* topk_idx, int64_t num_tokens,
+                                           int num_topk, int num_experts, int num_ranks,
+                                           int32_t* num_tokens_per_rank,
+                                           int32_t* num_tokens_per_expert,
+                                           uint8_t* is_token_in_rank, int32_t* slot,
+                                           int32_t* recv_base, int32_t* err_word,
+                                           ep_stream_t stream);
+
+/*
  * Copies P = recv_base[R] (device) into *host_total_rows and synchronises
  * `stream`.  The only synchronising call; use it to size the receive buffer
  * exactly, or skip it and pass a worst-case capacity of

@@ -24,6 +24,9 @@ bool device_props(DeviceProps* out) {
   if (cudaDeviceGetAttribute(&p.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
       cudaSuccess)
     return false;
+  if (cudaDeviceGetAttribute(&p.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+      cudaSuccess)
+    return false;
   if (dev < 64) {
     cache[dev] = p;
     have[dev] = true;

@@ -8,22 +8,30 @@
 // double buffered" pattern).  For every token t:
 //     out[t] = bf16_rne( sum_k w[t][k] * y[slot[t][rank(e_k)]] )   (float32)
 //
-// Design (one persistent CTA per SM, warp-specialised):
-//   - warp 0 is the producer.  For a batch of 32 tokens each lane gathers
-//     one token's routing: its distinct destination ranks (each row is read
-//     from HBM once, however many of the token's slots name that rank), the
-//     row index of every top-k slot inside the staged tile, and the
-//     weights.  Then, per (token, channel chunk), it waits for a free stage,
-//     publishes the slot->row map and weights, arrives on the stage's "full"
-//     mbarrier (all 32 lanes; lane 0 also posts the byte count) and issues
-//     one 1-D bulk copy per distinct row (lane j copies row j).
-//   - warps 1..8 are consumers: they wait on "full", accumulate the weighted
-//     rows in float32 from shared memory (8 channels per thread, one 16-byte
-//     shared load per slot), store 16 bytes of bf16 per thread, and release
-//     the stage on its "empty" mbarrier.
-//   - every wait is bounded (1 s); on a timeout the CTA records
-//     EP_ERRBIT_TIMEOUT, stops issuing, waits (bounded) for the copies it has
-//     in flight, and returns.
+// Design: persistent CTAs, several per SM, three warp roles per CTA, all
+// communication through mbarriers in shared memory.
+//   - warp 1 (routing): for batches of 32 tokens, each lane gathers one
+//     token's routing into a double-buffered table: the token's distinct
+//     destination rows (each row is read from HBM once, however many of the
+//     token's slots name that rank), the staged-row index of every top-k
+//     slot, and the weights.  Loads are issued eight at a time, and the warp
+//     runs one batch ahead of the copies.
+//   - warp 0 (copies): per (token, channel chunk) it waits for a free stage,
+//     posts the byte count on the stage's "full" barrier and issues one 1-D
+//     bulk copy per distinct row (lane j copies row j), with an L2
+//     evict-first policy (every row is read once).
+//   - warps 2..5 (reduce): wait on "full", accumulate the weighted rows in
+//     float32 from shared memory (8 channels per thread and pass, one 16-byte
+//     shared load per top-k slot), store 16 bytes of bf16 per thread, release
+//     the stage on its "empty" barrier, and a table once its batch is done.
+// Sizing: on GB300 one CTA's bulk-copy ring sustains about one stage per
+// memory round trip, so bandwidth comes from large stages (2048-channel
+// chunks, wider when min(K, R) is small) and from 3-4 CTAs per SM, not from
+// deep rings; the host picks the chunk, the stage count (2 or 3) and the
+// CTAs per SM from the shared-memory budget.
+// Every wait is bounded (1 s).  On a timeout the CTA records
+// EP_ERRBIT_TIMEOUT, stops issuing, waits (bounded) for the copies it has in
+// flight, and returns.
 #include <cuda_bf16.h>
 
 #include "ep_common.cuh"
@@ -31,17 +39,12 @@
 namespace ep {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kChunkMax = kConsumerWarps * 32 * 8;  // channels covered by one pass
-constexpr int kMaxStages = 16;
-constexpr int kBatch = 32;  // tokens gathered per producer round
-constexpr int kTabStride = EP_MAX_TOPK + 1;
-
-struct StageDesc {
-  float w[EP_MAX_TOPK];
-  int8_t j[EP_MAX_TOPK];  // staged row of each top-k slot, -1 = masked
-};
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kMaxStages = 3;
+constexpr int kBatch = 32;              // tokens per routing table
+constexpr int kTargetStageBytes = 16384;  // bytes a stage should carry at least
+constexpr int kMaxCtasPerSm = 4;
 
 struct Args {
   const uint16_t* y;
@@ -56,164 +59,245 @@ struct Args {
   int C;       // channels per chunk (multiple of 8)
   int nchunk;  // chunks per token
   int S;       // pipeline stages
+  int dmax;    // rows per stage = min(K, R)
   uint32_t stage_bytes;
 };
 
-// dynamic shared memory layout after the S row tiles
-struct Tail {
-  StageDesc desc[kMaxStages];
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
-  float tw[kBatch][kTabStride];
-  int32_t trow[kBatch][kTabStride];
-  int8_t tj[kBatch][kTabStride];
-  int32_t tD[kBatch];
-  int abort;
+// Offsets of the shared-memory regions that follow the S row tiles.
+struct SmemLayout {
+  size_t bars, rows, w, D, j, abort, total;
 };
+
+__host__ __device__ inline size_t al(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline SmemLayout smem_layout(int S, uint32_t stage_bytes, int K, int dmax) {
+  SmemLayout L;
+  size_t off = (size_t)S * stage_bytes;
+  L.bars = off;
+  off += sizeof(uint64_t) * (2 * (size_t)S + 4);
+  L.rows = off;
+  off += sizeof(int32_t) * 2 * kBatch * (size_t)dmax;
+  L.w = off;
+  off += sizeof(float) * 2 * kBatch * (size_t)K;
+  L.D = off;
+  off += sizeof(int32_t) * 2 * kBatch;
+  L.j = off;
+  off += 2 * kBatch * (size_t)K;
+  off = al(off, 16);
+  L.abort = off;
+  off += 16;
+  L.total = al(off, 128);
+  return L;
+}
 
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const volatile int* abort) {
   const bool got = mbar_wait_bounded(bar, parity, abort);
   return __all_sync(0xFFFFFFFFu, got);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) combine_kernel(Args a) {
+// One lane's token: distinct rows (in order of first appearance over k), the
+// staged-row index of every slot, and the weights.  Global loads are issued
+// eight slots at a time before any of them is used.
+__device__ __forceinline__ int gather_token(const Args& a, int64_t t, int32_t* rows, float* w,
+                                            int8_t* j, bool& bad) {
+  const int64_t* idx = a.topk_idx + t * a.K;
+  const float* wt = a.topk_w + t * a.K;
+  int D = 0;
+  for (int k0 = 0; k0 < a.K; k0 += 8) {
+    int64_t e[8];
+    float wv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int k = k0 + u;
+      e[u] = k < a.K ? idx[k] : -1;
+      wv[u] = k < a.K ? wt[k] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int k = k0 + u;
+      if (k >= a.K) break;
+      w[k] = wv[u];
+      int jj = -1;
+      if (e[u] >= 0 && e[u] < a.E) {
+        const int r = (int)(e[u] / a.El);
+        for (int q = 0; q < D; ++q)
+          if (rows[q] == r) jj = q;
+        if (jj < 0) {
+          jj = D;
+          rows[D++] = r;  // a rank for now; replaced by its row below
+        }
+      } else if (e[u] != -1) {
+        bad = true;
+      }
+      j[k] = (int8_t)jj;
+    }
+  }
+  const int32_t* srow = a.slot + t * a.R;
+  for (int q0 = 0; q0 < D; q0 += 8) {
+    int32_t v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = q0 + u < D ? srow[rows[q0 + u]] : 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (q0 + u < D) rows[q0 + u] = v[u];
+  }
+  return D;
+}
+
+__global__ void __launch_bounds__(kThreads, 3) combine_kernel(Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  const SmemLayout lay = smem_layout(a.S, a.stage_bytes, a.K, a.dmax);
   uint8_t* tiles = smem;
-  Tail& tl = *reinterpret_cast<Tail*>(smem + (size_t)a.S * a.stage_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
+  uint64_t* empty = full + a.S;
+  uint64_t* tfull = empty + a.S;  // [2] routing table ready
+  uint64_t* tempty = tfull + 2;   // [2] routing table released by the reducers
+  int32_t* trows = reinterpret_cast<int32_t*>(smem + lay.rows);  // [2][kBatch][dmax]
+  float* tw = reinterpret_cast<float*>(smem + lay.w);            // [2][kBatch][K]
+  int32_t* tD = reinterpret_cast<int32_t*>(smem + lay.D);        // [2][kBatch]
+  int8_t* tj = reinterpret_cast<int8_t*>(smem + lay.j);          // [2][kBatch][K]
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + lay.abort);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.S; ++s) {
-      mbar_init(&tl.full[s], 32);  // every producer lane arrives (releasing its writes)
-      mbar_init(&tl.empty[s], kConsumerWarps);
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
     }
-    tl.abort = 0;
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 32);
+      mbar_init(&tempty[b], kConsumerWarps);
+    }
+    *abort = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
-  volatile int* abort = &tl.abort;
-  const int64_t tb = a.T * blockIdx.x / gridDim.x;
-  const int64_t te = a.T * (blockIdx.x + 1) / gridDim.x;
+  // this CTA's tokens: whole batches of 32, spread evenly over the grid
+  const int64_t nbat = (a.T + kBatch - 1) / kBatch;
+  const int64_t b0 = nbat * blockIdx.x / gridDim.x;
+  const int64_t b1 = nbat * (blockIdx.x + 1) / gridDim.x;
+  const int64_t tb = b0 * kBatch;
+  const int64_t te = b1 * kBatch < a.T ? b1 * kBatch : a.T;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    const uint64_t policy = l2_policy_evict_first();
-    uint32_t it = 0;
+  if (warp == 1) {
+    // ------------------------------------------------------------ routing
     bool ok = true, bad = false;
-    for (int64_t t0 = tb; t0 < te && ok; t0 += kBatch) {
+    uint32_t bi = 0;
+    for (int64_t t0 = tb; t0 < te; t0 += kBatch, ++bi) {
+      const int buf = bi & 1;
+      const uint32_t use = bi >> 1;
+      if (use > 0 && !wait_warp(&tempty[buf], (use - 1) & 1, abort)) {
+        ok = false;
+        break;
+      }
       const int n = (int)(te - t0 < kBatch ? te - t0 : kBatch);
       if (lane < n) {
-        const int64_t t = t0 + lane;
-        int D = 0;
-        for (int k = 0; k < a.K; ++k) {
-          const int64_t e = a.topk_idx[t * a.K + k];
-          int j = -1;
-          if (e >= 0 && e < a.E) {
-            const int r = (int)(e / a.El);
-            for (int q = 0; q < D; ++q)
-              if (tl.trow[lane][q] == r) j = q;
-            if (j < 0) {
-              j = D++;
-              tl.trow[lane][j] = r;
-            }
-          } else if (e != -1) {
-            bad = true;
-          }
-          tl.tj[lane][k] = (int8_t)j;
-          tl.tw[lane][k] = a.topk_w[t * a.K + k];
-        }
-        for (int q = 0; q < D; ++q) tl.trow[lane][q] = a.slot[t * a.R + tl.trow[lane][q]];
-        tl.tD[lane] = D;
+        const size_t e = (size_t)buf * kBatch + lane;
+        tD[e] = gather_token(a, t0 + lane, trows + e * a.dmax, tw + e * a.K, tj + e * a.K, bad);
       }
-      __syncwarp();
+      mbar_arrive(&tfull[buf]);  // every lane releases its own table writes
+    }
+    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && a.err) atomicOr(a.err, EP_ERRBIT_BAD_EXPERT);
+    if (!ok && lane == 0) {
+      *abort = 1;
+      if (a.err) atomicOr(a.err, EP_ERRBIT_TIMEOUT);
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ copies
+    const uint64_t policy = l2_policy_evict_first();
+    uint32_t it = 0, bi = 0;
+    bool ok = true;
+    for (int64_t t0 = tb; t0 < te && ok; t0 += kBatch, ++bi) {
+      const int buf = bi & 1;
+      if (!wait_warp(&tfull[buf], (bi >> 1) & 1, abort)) {
+        ok = false;
+        break;
+      }
+      const int n = (int)(te - t0 < kBatch ? te - t0 : kBatch);
       for (int i = 0; i < n && ok; ++i) {
-        const int D = tl.tD[i];
-        const int64_t t = t0 + i;
-        (void)t;
+        const size_t e = (size_t)buf * kBatch + i;
+        const int D = tD[e];
+        const int64_t row = lane < D ? trows[e * a.dmax + lane] : 0;
         for (int c = 0; c < a.nchunk; ++c) {
           const uint32_t s = it % a.S, use = it / a.S;
-          if (use > 0 && !wait_warp(&tl.empty[s], (use - 1) & 1, abort)) {
+          if (use > 0 && !wait_warp(&empty[s], (use - 1) & 1, abort)) {
             ok = false;
             break;
           }
-          if (lane < a.K) {
-            tl.desc[s].j[lane] = tl.tj[i][lane];
-            tl.desc[s].w[lane] = tl.tw[i][lane];
-          }
-          __syncwarp();
           const int c0 = c * a.C;
           const int clen = min(a.C, a.H - c0);
-          if (lane == 0)
-            mbar_arrive_expect_tx(&tl.full[s], (uint32_t)(D * clen * 2));
-          else
-            mbar_arrive(&tl.full[s]);
+          if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(D * clen * 2));
           __syncwarp();
           if (lane < D)
             bulk_load_g2s(tiles + (size_t)s * a.stage_bytes + (size_t)lane * a.C * 2,
-                          a.y + (int64_t)tl.trow[i][lane] * a.H + c0, (uint32_t)clen * 2,
-                          &tl.full[s], policy);
+                          a.y + row * a.H + c0, (uint32_t)clen * 2, &full[s], policy);
           ++it;
         }
       }
-      __syncwarp();
     }
-    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && a.err) atomicOr(a.err, EP_ERRBIT_BAD_EXPERT);
-    if (!ok) {
-      if (lane == 0) {
-        *abort = 1;
-        if (a.err) atomicOr(a.err, EP_ERRBIT_TIMEOUT);
-      }
+    if (!ok && lane == 0) {
+      *abort = 1;
+      if (a.err) atomicOr(a.err, EP_ERRBIT_TIMEOUT);
     }
     // Copies still in flight must land before the CTA may exit: wait for the
     // last fill of every stage (bounded, and regardless of the abort flag).
     const int zero = 0;
     const uint32_t first = it > (uint32_t)a.S ? it - (uint32_t)a.S : 0u;
     for (uint32_t u = first; u < it; ++u)
-      (void)mbar_wait_bounded(&tl.full[u % a.S], (u / a.S) & 1, &zero);
+      (void)mbar_wait_bounded(&full[u % a.S], (u / a.S) & 1, &zero);
   } else {
-    // ------------------------------------------------------------ consumers
-    const int ct = threadIdx.x - 32;
-    uint32_t it = 0;
+    // ------------------------------------------------------------ reduce
+    const int ct = threadIdx.x - 64;
+    uint32_t it = 0, bi = 0;
     bool ok = true;
-    for (int64_t t = tb; t < te && ok; ++t) {
-      uint16_t* orow = a.out + t * a.H;
-      for (int c = 0; c < a.nchunk; ++c) {
-        const uint32_t s = it % a.S;
-        if (!wait_warp(&tl.full[s], (it / a.S) & 1, abort)) {
-          ok = false;
-          break;
-        }
-        const int c0 = c * a.C;
-        const int clen = min(a.C, a.H - c0);
-        const uint8_t* stage = tiles + (size_t)s * a.stage_bytes;
-        for (int ch = ct * 8; ch < clen; ch += kConsumerWarps * 32 * 8) {
-          float acc[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-          for (int k = 0; k < a.K; ++k) {
-            const int j = tl.desc[s].j[k];
-            if (j < 0) continue;
-            const float w = tl.desc[s].w[k];
-            const int4 v = *reinterpret_cast<const int4*>(stage + ((size_t)j * a.C + ch) * 2);
-            float f[8];
-            unpack_bf16x8(v, f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, f[i], acc[i]);
+    for (int64_t t0 = tb; t0 < te && ok; t0 += kBatch, ++bi) {
+      const int buf = bi & 1;
+      const int n = (int)(te - t0 < kBatch ? te - t0 : kBatch);
+      for (int i = 0; i < n && ok; ++i) {
+        const size_t e = (size_t)buf * kBatch + i;
+        const int8_t* j = tj + e * a.K;
+        const float* w = tw + e * a.K;
+        uint16_t* orow = a.out + (t0 + i) * a.H;
+        for (int c = 0; c < a.nchunk; ++c) {
+          const uint32_t s = it % a.S;
+          if (!wait_warp(&full[s], (it / a.S) & 1, abort)) {
+            ok = false;
+            break;
           }
-          int4 o;
-          uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+          const int c0 = c * a.C;
+          const int clen = min(a.C, a.H - c0);
+          const uint8_t* stage = tiles + (size_t)s * a.stage_bytes;
+          for (int ch = ct * 8; ch < clen; ch += kConsumerWarps * 32 * 8) {
+            float acc[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 p = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-            ow[i] = *reinterpret_cast<const uint32_t*>(&p);
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+            for (int k = 0; k < a.K; ++k) {
+              const int jk = j[k];
+              if (jk < 0) continue;
+              const float wk = w[k];
+              const int4 v = *reinterpret_cast<const int4*>(stage + ((size_t)jk * a.C + ch) * 2);
+              float f[8];
+              unpack_bf16x8(v, f);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) acc[q] = fmaf(wk, f[q], acc[q]);
+            }
+            int4 o;
+            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const __nv_bfloat162 p = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+              ow[q] = *reinterpret_cast<const uint32_t*>(&p);
+            }
+            *reinterpret_cast<int4*>(orow + c0 + ch) = o;
           }
-          *reinterpret_cast<int4*>(orow + c0 + ch) = o;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+          ++it;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tl.empty[s]);
-        ++it;
       }
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(&tempty[buf]);
     }
     if (!ok && lane == 0) {
       *abort = 1;
@@ -222,31 +306,44 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(Args a) {
   }
 }
 
-size_t tail_bytes() { return align_up(sizeof(Tail), 128); }
+struct Plan {
+  int C, S, ctas_per_sm;
+  uint32_t stage_bytes;
+  size_t smem;
+};
 
-}  // namespace
-
-bool combine_plan(int H, int K, int R, int smem_optin, int* C, int* S, uint32_t* stage_bytes) {
+// Chunk, stage count and CTAs per SM for a shape: stages of at least
+// kTargetStageBytes when min(K,R) rows are staged, as many CTAs per SM (up
+// to 4) as the shared memory allows, and 3 stages where they still fit.
+bool make_plan(int H, int K, int R, const DeviceProps& p, Plan* out) {
   const int dmax = K < R ? K : R;
-  const long budget = (long)smem_optin - (long)tail_bytes();
-  if (budget <= 0) return false;
-  int c = H < kChunkMax ? H : kChunkMax;
-  long sb = (long)dmax * c * 2;
-  while (sb * 4 > budget && c > 256) {
-    c = (c / 2 + 7) / 8 * 8;
-    sb = (long)dmax * c * 2;
+  const int reserve = 1024;  // per-block shared memory the runtime keeps
+  int c = kTargetStageBytes / (2 * dmax);
+  c = c < 2048 ? 2048 : c;
+  c = (c + 7) / 8 * 8;
+  if (c > H) c = H;
+  for (; c >= 8; c = (c / 2 + 7) / 8 * 8) {
+    const uint32_t sb = (uint32_t)al((size_t)dmax * c * 2, 128);
+    for (int cps = kMaxCtasPerSm; cps >= 1; --cps) {
+      const long per_cta = (long)p.smem_per_sm / cps - reserve;
+      for (int S = kMaxStages; S >= 2; --S) {
+        const size_t need = smem_layout(S, sb, K, dmax).total;
+        if ((long)need <= per_cta && (long)need <= (long)p.smem_optin) {
+          out->C = c;
+          out->S = S;
+          out->ctas_per_sm = cps;
+          out->stage_bytes = sb;
+          out->smem = need;
+          return true;
+        }
+      }
+    }
+    if (c == 8) break;
   }
-  long s = budget / sb;
-  if (s > kMaxStages) s = kMaxStages;
-  if (s < 2) return false;
-  *C = c;
-  *S = (int)s;
-  *stage_bytes = (uint32_t)align_up((size_t)sb, 128);
-  // recheck with the aligned tile size
-  if ((long)*stage_bytes * *S > budget) *S = (int)(budget / *stage_bytes);
-  return *S >= 2;
+  return false;
 }
 
+}  // namespace
 }  // namespace ep
 
 using namespace ep;
@@ -262,6 +359,8 @@ extern "C" ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk
   if (!aligned16(y) || !aligned16(out)) return EP_ERR_INVALID_ARG;
   DeviceProps props;
   if (!device_props(&props)) return EP_ERR_CUDA;
+  Plan plan;
+  if (!make_plan(hidden, num_topk, num_ranks, props, &plan)) return EP_ERR_INVALID_ARG;
   Args a;
   a.y = static_cast<const uint16_t*>(y);
   a.out = static_cast<uint16_t*>(out);
@@ -275,14 +374,22 @@ extern "C" ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk
   a.R = num_ranks;
   a.slot = slot;
   a.err = err_word;
-  if (!combine_plan(hidden, num_topk, num_ranks, props.smem_optin, &a.C, &a.S, &a.stage_bytes))
-    return EP_ERR_INVALID_ARG;
+  a.dmax = num_topk < num_ranks ? num_topk : num_ranks;
+  a.C = plan.C;
+  a.S = plan.S;
+  a.stage_bytes = plan.stage_bytes;
   a.nchunk = (hidden + a.C - 1) / a.C;
-  const size_t smem = (size_t)a.S * a.stage_bytes + tail_bytes();
   if (cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+                           (int)plan.smem) != cudaSuccess)
     return EP_ERR_CUDA;
-  const int64_t grid = num_tokens < props.sm_count ? num_tokens : props.sm_count;
-  combine_kernel<<<(unsigned)grid, kThreads, smem, to_cuda(stream)>>>(a);
+  int resident = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, combine_kernel, kThreads,
+                                                    plan.smem) != cudaSuccess)
+    return EP_ERR_CUDA;
+  if (resident < 1) return EP_ERR_CUDA;
+  const int64_t ctas = (int64_t)props.sm_count * (resident < plan.ctas_per_sm ? resident : plan.ctas_per_sm);
+  const int64_t nbat = (num_tokens + kBatch - 1) / kBatch;
+  const int64_t grid = nbat < ctas ? nbat : ctas;
+  combine_kernel<<<(unsigned)grid, kThreads, plan.smem, to_cuda(stream)>>>(a);
   return launch_status();
 }

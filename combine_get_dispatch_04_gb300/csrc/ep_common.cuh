@@ -27,7 +27,8 @@ inline ep_status_t launch_status() {
 
 struct DeviceProps {
   int sm_count = 0;
-  int smem_optin = 0;  // max dynamic shared memory per block (opt-in)
+  int smem_optin = 0;   // max dynamic shared memory per block (opt-in)
+  int smem_per_sm = 0;  // shared memory per SM, shared by its resident blocks
 };
 
 // Cached per device; returns false if the CUDA runtime cannot be queried.

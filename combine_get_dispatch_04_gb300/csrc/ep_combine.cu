@@ -173,12 +173,9 @@ __global__ void __launch_bounds__(kThreads, 3) combine_kernel(Args a) {
   }
   __syncthreads();
 
-  // this CTA's tokens: whole batches of 32, spread evenly over the grid
-  const int64_t nbat = (a.T + kBatch - 1) / kBatch;
-  const int64_t b0 = nbat * blockIdx.x / gridDim.x;
-  const int64_t b1 = nbat * (blockIdx.x + 1) / gridDim.x;
-  const int64_t tb = b0 * kBatch;
-  const int64_t te = b1 * kBatch < a.T ? b1 * kBatch : a.T;
+  // this CTA's tokens: a contiguous range, balanced to within one token
+  const int64_t tb = a.T * blockIdx.x / gridDim.x;
+  const int64_t te = a.T * (blockIdx.x + 1) / gridDim.x;
 
   if (warp == 1) {
     // ------------------------------------------------------------ routing
@@ -388,8 +385,7 @@ extern "C" ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk
     return EP_ERR_CUDA;
   if (resident < 1) return EP_ERR_CUDA;
   const int64_t ctas = (int64_t)props.sm_count * (resident < plan.ctas_per_sm ? resident : plan.ctas_per_sm);
-  const int64_t nbat = (num_tokens + kBatch - 1) / kBatch;
-  const int64_t grid = nbat < ctas ? nbat : ctas;
+  const int64_t grid = num_tokens < ctas ? num_tokens : ctas;
   combine_kernel<<<(unsigned)grid, kThreads, plan.smem, to_cuda(stream)>>>(a);
   return launch_status();
 }

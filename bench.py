@@ -8,7 +8,7 @@ synthetic routing and hidden states, on one GB300 per process.
 Prints one JSON line (rank 0).  `value` is whole-job tokens/s with inputs
 resident in HBM; `e2e` is the same metric with the step's inputs copied from
 pinned host memory and the combined output copied back inside the timed
-region.  Multi-GPU runs (torchrun) are independent replicas, one problem per
+region (pipelined over token chunks on two copy streams).  Multi-GPU runs (torchrun) are independent replicas, one problem per
 GPU (the shuffle on one GPU has no cross-GPU step): per-GPU work is fixed,
 value = N * T / max-over-ranks step time.
 
@@ -366,13 +366,42 @@ def run_ours(args, cfg: Config):
     h_x = torch.from_numpy(case.x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
     h_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     e2e_steps = max(1, min(args.steps, 20))
+    # The step through the public API on host buffers, pipelined over token
+    # chunks: routing in -> layout; then per chunk, x in (copy stream) ->
+    # dispatch + combine of that chunk's tokens (compute stream) -> out back
+    # (second copy stream).  Every step moves all inputs in and the whole
+    # result out.
+    n_chunks = max(1, min(args.e2e_chunks, T // 8192))  # chunks of at least 8192 tokens
+    bounds = [T * i // n_chunks for i in range(n_chunks + 1)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(n_chunks)]
+    ev_done = [torch.cuda.Event() for _ in range(n_chunks)]
+    ev_begin, ev_back = torch.cuda.Event(), torch.cuda.Event()
+    from dataclasses import replace as _replace
 
     def e2e_step():
+        ev_begin.record(stream)
         idx.copy_(h_idx, non_blocking=True)
         w.copy_(h_w, non_blocking=True)
-        x.copy_(h_x, non_blocking=True)
-        step()
-        h_out.copy_(out, non_blocking=True)
+        s_in.wait_event(ev_begin)
+        for c in range(n_chunks):
+            a, b = bounds[c], bounds[c + 1]
+            with torch.cuda.stream(s_in):
+                x[a:b].copy_(h_x[a:b], non_blocking=True)
+                ev_in[c].record(s_in)
+        ep.get_dispatch_layout(idx, E, R, err=err, out=L)
+        for c in range(n_chunks):
+            a, b = bounds[c], bounds[c + 1]
+            stream.wait_event(ev_in[c])
+            Lc = _replace(L, slot=L.slot[a:b], is_token_in_rank=L.is_token_in_rank[a:b])
+            ep.dispatch(x[a:b], idx[a:b], w[a:b], Lc, use_fp8=cfg.fp8, err=err, out=D)
+            ep.combine(Y, idx[a:b], w[a:b], Lc, err=err, out=out[a:b])
+            ev_done[c].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[c])
+                h_out[a:b].copy_(out[a:b], non_blocking=True)
+        ev_back.record(s_out)
+        stream.wait_event(ev_back)
 
     e2e_step()
     torch.cuda.synchronize(dev)
@@ -386,6 +415,11 @@ def run_ours(args, cfg: Config):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+    # the pipelined steps must give the resident step's result, bit for bit
+    step()
+    torch.cuda.synchronize(dev)
+    e2e_check = "out matches the device-resident step" if torch.equal(
+        h_out.view(torch.int16), out.cpu().view(torch.int16)) else "MISMATCH"
     h2d = h_idx.numel() * 8 + h_w.numel() * 4 + h_x.numel() * 2
     d2h = h_out.numel() * 2
     if int(err.item()) != 0:
@@ -425,7 +459,8 @@ def run_ours(args, cfg: Config):
             "kernels": kern,
             "e2e": {"value": whole_job_tokens_per_s(T, world, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "steps": e2e_steps},
+                    "steps": e2e_steps, "token_chunks": n_chunks,
+                    "check": e2e_check},
             "gpu_launches": 5 * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
@@ -446,6 +481,8 @@ def main(argv=None):
     ap.add_argument("--tokens-per-rank", type=int, default=None,
                     help="scale the workload (same recipe) for profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=8,
+                    help="token chunks the end-to-end step pipelines its copies over")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

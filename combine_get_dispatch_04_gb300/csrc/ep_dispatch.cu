@@ -7,9 +7,10 @@
 // a memory-bound copy: each token row is read once from HBM and written once
 // per destination rank.
 //
-// One warp per token.  Lanes hold 16-byte vectors of the row (8 bf16
-// channels); kUnroll vectors per lane are loaded before the stores so each
-// warp keeps 4 x 512 bytes of reads in flight.  Loads bypass L1, stores use
+// One warp per token, or per slice of a token when the batch is too small
+// to fill the GPU (slices of a multiple of 32 vectors).  Lanes hold 16-byte
+// vectors of the row (8 bf16 channels); kUnroll vectors per lane are loaded
+// before the stores so each warp keeps 4 x 512 bytes of reads in flight.  Loads bypass L1, stores use
 // the streaming policy.  In the FP8 variant a half-warp holds one block of
 // 128 channels: its amax is a 4-step xor-shuffle reduction, and the block is
 // quantised in registers before being written to every destination.  The
@@ -44,6 +45,8 @@ struct Args {
   float* recv_topk_w;
   int32_t* nrpe;
   int32_t* err;
+  int nslices;  // warps per token
+  int vps;      // 16-byte vectors per slice (a multiple of 32)
 };
 
 __device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float d) {
@@ -67,7 +70,9 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_kernel(Args a) {
     }
   }
 
-  const int64_t t = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t t = gw / a.nslices;
+  const int slice = (int)(gw % a.nslices);
   if (t >= a.T) return;  // uniform per warp
 
   // destinations of this token, in rank order
@@ -92,7 +97,7 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_kernel(Args a) {
 
   // per-row metadata: source token, and the top-k entries that are local to
   // the destination (local expert id and weight), -1 / 0 elsewhere
-  if (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_w) {
+  if (slice == 0 && (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_w)) {
     const int64_t e = lane < a.K ? a.topk_idx[t * a.K + lane] : -1;
     const float w = (lane < a.K && a.topk_w) ? a.topk_w[t * a.K + lane] : 0.0f;
     const int er = (e >= 0 && e < a.E) ? (int)(e / a.El) : -1;
@@ -110,36 +115,40 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_kernel(Args a) {
 
   const int nvec = a.H / 8;  // 16-byte vectors per row
   const int4* src = a.x + t * nvec;
+  // this warp's slice of the row: [vbeg, vend), vbeg a multiple of 32 vectors
+  const int vbeg = slice * a.vps;
+  const int vend = min(nvec, vbeg + a.vps);
   if constexpr (!kFP8) {
     int4* out = reinterpret_cast<int4*>(a.recv_x);
-    for (int v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
+    for (int v0 = vbeg; v0 < vend; v0 += 32 * kUnroll) {
       int4 buf[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int v = v0 + u * 32 + lane;
-        if (v < nvec) buf[u] = ld_stream_v4(src + v);
+        if (v < vend) buf[u] = ld_stream_v4(src + v);
       }
       for (int d = 0; d < nd; ++d) {
         int4* dst = out + (int64_t)dst_row[warp][d] * nvec;
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int v = v0 + u * 32 + lane;
-          if (v < nvec) st_stream_v4(dst + v, buf[u]);
+          if (v < vend) st_stream_v4(dst + v, buf[u]);
         }
       }
     }
   } else {
-    // H % 128 == 0, so nvec % 16 == 0 and half-warps are wholly in or out
+    // H % 128 == 0 and vbeg % 32 == 0, so vend % 16 == 0: half-warps (one
+    // 128-channel block each) are wholly in or out
     uint8_t* out = reinterpret_cast<uint8_t*>(a.recv_x);
     const int nblk = a.H / 128;
-    for (int v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
+    for (int v0 = vbeg; v0 < vend; v0 += 32 * kUnroll) {
       uint2 q[kUnroll];
       float scale[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int v = v0 + u * 32 + lane;
         float f[8];
-        const int4 raw = v < nvec ? ld_stream_v4(src + v) : make_int4(0, 0, 0, 0);
+        const int4 raw = v < vend ? ld_stream_v4(src + v) : make_int4(0, 0, 0, 0);
         unpack_bf16x8(raw, f);
         float amax = 0.0f;
 #pragma unroll
@@ -161,7 +170,7 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_kernel(Args a) {
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int v = v0 + u * 32 + lane;
-          if (v < nvec) {
+          if (v < vend) {
             st_stream_v2(reinterpret_cast<uint2*>(dst + (int64_t)v * 8), q[u]);
             if ((lane & 15) == 0) srow[v >> 4] = scale[u];
           }
@@ -215,7 +224,18 @@ extern "C" ep_status_t ep_dispatch(const void* x, int hidden, const int64_t* top
   a.recv_topk_w = recv_topk_weights;
   a.nrpe = num_recv_tokens_per_expert;
   a.err = err_word;
-  int64_t blocks = (num_tokens + kWarps - 1) / kWarps;
+  // Small batches: several warps share a token (each a run of 32*kUnroll
+  // vectors), aiming at four waves of 64 warps per SM.
+  DeviceProps props;
+  if (!device_props(&props)) return EP_ERR_CUDA;
+  const int nvec = hidden / 8;
+  const int max_slices = (nvec + 32 * kUnroll - 1) / (32 * kUnroll);
+  const int64_t want_warps = (int64_t)props.sm_count * 64 * 4;
+  int64_t ns = num_tokens > 0 ? (want_warps + num_tokens - 1) / num_tokens : 1;
+  a.nslices = (int)(ns < 1 ? 1 : (ns > max_slices ? max_slices : ns));
+  a.vps = ((nvec + a.nslices - 1) / a.nslices + 31) / 32 * 32;
+  a.nslices = (nvec + a.vps - 1) / a.vps;  // no empty slice
+  int64_t blocks = (num_tokens * a.nslices + kWarps - 1) / kWarps;
   if (blocks == 0) {
     if (!a.nrpe) return EP_OK;
     blocks = 1;

@@ -13,17 +13,21 @@
 //   - warp 1 (routing): for batches of 32 tokens, each lane gathers one
 //     token's routing into a double-buffered table: the token's distinct
 //     destination rows (each row is read from HBM once, however many of the
-//     token's slots name that rank), the staged-row index of every top-k
-//     slot, and the weights.  Loads are issued eight at a time, and the warp
-//     runs one batch ahead of the copies.
+//     token's slots name that rank) and, per row, the sum of the weights of
+//     the slots naming its rank.  Loads are issued eight at a time, and the
+//     warp runs one batch ahead of the copies.
 //   - warp 0 (copies): per (token, channel chunk) it waits for a free stage,
 //     posts the byte count on the stage's "full" barrier and issues one 1-D
 //     bulk copy per distinct row (lane j copies row j), with an L2
 //     evict-first policy (every row is read once).
 //   - warps 2..5 (reduce): wait on "full", accumulate the weighted rows in
-//     float32 from shared memory (8 channels per thread and pass, one 16-byte
-//     shared load per top-k slot), store 16 bytes of bf16 per thread, release
-//     the stage on its "empty" barrier, and a table once its batch is done.
+//     float32 from shared memory (8 channels per thread and pass; the D
+//     16-byte shared loads of a pass are independent and issued together),
+//     store 16 bytes of bf16 per thread, release the stage on its "empty"
+//     barrier, and a table once its batch is done.
+// Each slot contributes w_k * y_row; slots naming the same rank share one
+// staged row, so their weights are summed first (the same sum, with the
+// float32 rounding applied in a different order).
 // Sizing: on GB300 one CTA's bulk-copy ring sustains about one stage per
 // memory round trip, so bandwidth comes from large stages (2048-channel
 // chunks, wider when min(K, R) is small) and from 3-4 CTAs per SM, not from
@@ -65,12 +69,12 @@ struct Args {
 
 // Offsets of the shared-memory regions that follow the S row tiles.
 struct SmemLayout {
-  size_t bars, rows, w, D, j, abort, total;
+  size_t bars, rows, w, D, abort, total;
 };
 
 __host__ __device__ inline size_t al(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline SmemLayout smem_layout(int S, uint32_t stage_bytes, int K, int dmax) {
+__host__ __device__ inline SmemLayout smem_layout(int S, uint32_t stage_bytes, int dmax) {
   SmemLayout L;
   size_t off = (size_t)S * stage_bytes;
   L.bars = off;
@@ -78,11 +82,9 @@ __host__ __device__ inline SmemLayout smem_layout(int S, uint32_t stage_bytes, i
   L.rows = off;
   off += sizeof(int32_t) * 2 * kBatch * (size_t)dmax;
   L.w = off;
-  off += sizeof(float) * 2 * kBatch * (size_t)K;
+  off += sizeof(float) * 2 * kBatch * (size_t)dmax;
   L.D = off;
   off += sizeof(int32_t) * 2 * kBatch;
-  L.j = off;
-  off += 2 * kBatch * (size_t)K;
   off = al(off, 16);
   L.abort = off;
   off += 16;
@@ -95,11 +97,11 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xFFFFFFFFu, got);
 }
 
-// One lane's token: distinct rows (in order of first appearance over k), the
-// staged-row index of every slot, and the weights.  Global loads are issued
-// eight slots at a time before any of them is used.
-__device__ __forceinline__ int gather_token(const Args& a, int64_t t, int32_t* rows, float* w,
-                                            int8_t* j, bool& bad) {
+// One lane's token: its distinct source rows (in order of first appearance
+// over k) and, per row, the sum of the weights of the slots that name its
+// rank.  Global loads are issued eight slots at a time before any is used.
+__device__ __forceinline__ int gather_token(const Args& a, int64_t t, int32_t* rows, float* W,
+                                            bool& bad) {
   const int64_t* idx = a.topk_idx + t * a.K;
   const float* wt = a.topk_w + t * a.K;
   int D = 0;
@@ -114,22 +116,21 @@ __device__ __forceinline__ int gather_token(const Args& a, int64_t t, int32_t* r
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int k = k0 + u;
-      if (k >= a.K) break;
-      w[k] = wv[u];
-      int jj = -1;
+      if (k0 + u >= a.K) break;
       if (e[u] >= 0 && e[u] < a.E) {
         const int r = (int)(e[u] / a.El);
+        int jj = -1;
         for (int q = 0; q < D; ++q)
           if (rows[q] == r) jj = q;
         if (jj < 0) {
-          jj = D;
-          rows[D++] = r;  // a rank for now; replaced by its row below
+          rows[D] = r;  // a rank for now; replaced by its row below
+          W[D++] = wv[u];
+        } else {
+          W[jj] += wv[u];
         }
       } else if (e[u] != -1) {
         bad = true;
       }
-      j[k] = (int8_t)jj;
     }
   }
   const int32_t* srow = a.slot + t * a.R;
@@ -144,18 +145,62 @@ __device__ __forceinline__ int gather_token(const Args& a, int64_t t, int32_t* r
   return D;
 }
 
-__global__ void __launch_bounds__(kThreads, 3) combine_kernel(Args a) {
+// out[ch..ch+8) of one staged (token, chunk): sum over the token's D staged
+// rows of W[d] * row_d, in float32.  With kDMax > 0 (D <= kDMax) the D shared
+// loads are issued back to back from unrolled code; kDMax == 0 is the
+// general loop.
+template <int kDMax>
+__device__ __forceinline__ int4 reduce_rows(const uint8_t* stage, int C, int ch, int D,
+                                            const float* Wreg, const float* Wsm) {
+  float acc[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+  if constexpr (kDMax > 0) {
+    int4 v[kDMax];
+#pragma unroll
+    for (int d = 0; d < kDMax; ++d)
+      if (d < D) v[d] = *reinterpret_cast<const int4*>(stage + ((size_t)d * C + ch) * 2);
+#pragma unroll
+    for (int d = 0; d < kDMax; ++d) {
+      if (d < D) {
+        float f[8];
+        unpack_bf16x8(v[d], f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = fmaf(Wreg[d], f[q], acc[q]);
+      }
+    }
+  } else {
+    for (int d = 0; d < D; ++d) {
+      const int4 v = *reinterpret_cast<const int4*>(stage + ((size_t)d * C + ch) * 2);
+      const float wd = Wsm[d];
+      float f[8];
+      unpack_bf16x8(v, f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(wd, f[q], acc[q]);
+    }
+  }
+  int4 o;
+  uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __nv_bfloat162 p = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+    ow[q] = *reinterpret_cast<const uint32_t*>(&p);
+  }
+  return o;
+}
+
+template <int kDMax>
+__global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const SmemLayout lay = smem_layout(a.S, a.stage_bytes, a.K, a.dmax);
+  const SmemLayout lay = smem_layout(a.S, a.stage_bytes, a.dmax);
   uint8_t* tiles = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
   uint64_t* empty = full + a.S;
   uint64_t* tfull = empty + a.S;  // [2] routing table ready
   uint64_t* tempty = tfull + 2;   // [2] routing table released by the reducers
   int32_t* trows = reinterpret_cast<int32_t*>(smem + lay.rows);  // [2][kBatch][dmax]
-  float* tw = reinterpret_cast<float*>(smem + lay.w);            // [2][kBatch][K]
+  float* tW = reinterpret_cast<float*>(smem + lay.w);            // [2][kBatch][dmax]
   int32_t* tD = reinterpret_cast<int32_t*>(smem + lay.D);        // [2][kBatch]
-  int8_t* tj = reinterpret_cast<int8_t*>(smem + lay.j);          // [2][kBatch][K]
   volatile int* abort = reinterpret_cast<volatile int*>(smem + lay.abort);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
@@ -191,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 3) combine_kernel(Args a) {
       const int n = (int)(te - t0 < kBatch ? te - t0 : kBatch);
       if (lane < n) {
         const size_t e = (size_t)buf * kBatch + lane;
-        tD[e] = gather_token(a, t0 + lane, trows + e * a.dmax, tw + e * a.K, tj + e * a.K, bad);
+        tD[e] = gather_token(a, t0 + lane, trows + e * a.dmax, tW + e * a.dmax, bad);
       }
       mbar_arrive(&tfull[buf]);  // every lane releases its own table writes
     }
@@ -253,8 +298,9 @@ __global__ void __launch_bounds__(kThreads, 3) combine_kernel(Args a) {
       const int n = (int)(te - t0 < kBatch ? te - t0 : kBatch);
       for (int i = 0; i < n && ok; ++i) {
         const size_t e = (size_t)buf * kBatch + i;
-        const int8_t* j = tj + e * a.K;
-        const float* w = tw + e * a.K;
+        const float* Wsm = tW + e * a.dmax;
+        float Wreg[kDMax > 0 ? kDMax : 1];
+        int D = 0;
         uint16_t* orow = a.out + (t0 + i) * a.H;
         for (int c = 0; c < a.nchunk; ++c) {
           const uint32_t s = it % a.S;
@@ -262,32 +308,17 @@ __global__ void __launch_bounds__(kThreads, 3) combine_kernel(Args a) {
             ok = false;
             break;
           }
+          if (c == 0) {  // the table entry is visible once the token's first stage is
+            D = tD[e];
+#pragma unroll
+            for (int d = 0; d < (kDMax > 0 ? kDMax : 1); ++d) Wreg[d] = d < D ? Wsm[d] : 0.0f;
+          }
           const int c0 = c * a.C;
           const int clen = min(a.C, a.H - c0);
           const uint8_t* stage = tiles + (size_t)s * a.stage_bytes;
-          for (int ch = ct * 8; ch < clen; ch += kConsumerWarps * 32 * 8) {
-            float acc[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-            for (int k = 0; k < a.K; ++k) {
-              const int jk = j[k];
-              if (jk < 0) continue;
-              const float wk = w[k];
-              const int4 v = *reinterpret_cast<const int4*>(stage + ((size_t)jk * a.C + ch) * 2);
-              float f[8];
-              unpack_bf16x8(v, f);
-#pragma unroll
-              for (int q = 0; q < 8; ++q) acc[q] = fmaf(wk, f[q], acc[q]);
-            }
-            int4 o;
-            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const __nv_bfloat162 p = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-              ow[q] = *reinterpret_cast<const uint32_t*>(&p);
-            }
-            *reinterpret_cast<int4*>(orow + c0 + ch) = o;
-          }
+          for (int ch = ct * 8; ch < clen; ch += kConsumerWarps * 32 * 8)
+            *reinterpret_cast<int4*>(orow + c0 + ch) =
+                reduce_rows<kDMax>(stage, a.C, ch, D, Wreg, Wsm);
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);
           ++it;
@@ -324,7 +355,7 @@ bool make_plan(int H, int K, int R, const DeviceProps& p, Plan* out) {
     for (int cps = kMaxCtasPerSm; cps >= 1; --cps) {
       const long per_cta = (long)p.smem_per_sm / cps - reserve;
       for (int S = kMaxStages; S >= 2; --S) {
-        const size_t need = smem_layout(S, sb, K, dmax).total;
+        const size_t need = smem_layout(S, sb, dmax).total;
         if ((long)need <= per_cta && (long)need <= (long)p.smem_optin) {
           out->C = c;
           out->S = S;
@@ -376,16 +407,18 @@ extern "C" ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk
   a.S = plan.S;
   a.stage_bytes = plan.stage_bytes;
   a.nchunk = (hidden + a.C - 1) / a.C;
-  if (cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // rows per token <= 8 (every workload here): unrolled reduction
+  void (*kernel)(Args) = a.dmax <= 8 ? combine_kernel<8> : combine_kernel<0>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)plan.smem) != cudaSuccess)
     return EP_ERR_CUDA;
   int resident = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, combine_kernel, kThreads,
-                                                    plan.smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, kThreads, plan.smem) !=
+      cudaSuccess)
     return EP_ERR_CUDA;
   if (resident < 1) return EP_ERR_CUDA;
   const int64_t ctas = (int64_t)props.sm_count * (resident < plan.ctas_per_sm ? resident : plan.ctas_per_sm);
   const int64_t grid = num_tokens < ctas ? num_tokens : ctas;
-  combine_kernel<<<(unsigned)grid, kThreads, plan.smem, to_cuda(stream)>>>(a);
+  kernel<<<(unsigned)grid, kThreads, plan.smem, to_cuda(stream)>>>(a);
   return launch_status();
 }

@@ -106,20 +106,27 @@ __global__ void __launch_bounds__(kTok)
   uint64_t mask = 0;
   bool bad = false;
   const int64_t* row = topk_idx + t * g.K;
-  for (int k = 0; k < g.K; ++k) {
-    const int64_t e = valid ? row[k] : -1;
-    int key = -1;
-    if (e != -1) {
-      if (e < -1 || e >= g.E) {
-        bad = true;
-      } else {
-        key = (int)e;
-        mask |= 1ull << (key / g.El);
+  for (int k0 = 0; k0 < g.K; k0 += 8) {
+    int64_t ev[8];  // eight ids loaded before any is used
+#pragma unroll
+    for (int u = 0; u < 8; ++u) ev[u] = (valid && k0 + u < g.K) ? row[k0 + u] : -1;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (k0 + u >= g.K) break;  // uniform: every lane runs the same slots
+      const int64_t e = ev[u];
+      int key = -1;
+      if (e != -1) {
+        if (e < -1 || e >= g.E) {
+          bad = true;
+        } else {
+          key = (int)e;
+          mask |= 1ull << (key / g.El);
+        }
       }
+      // lanes naming the same expert add once, through their lowest lane
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, key);
+      if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[key], __popc(peers));
     }
-    // lanes naming the same expert add once, through their lowest lane
-    const unsigned peers = __match_any_sync(0xFFFFFFFFu, key);
-    if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[key], __popc(peers));
   }
   if (valid) {
     ws.masks[t] = mask;
@@ -210,9 +217,23 @@ __global__ void __launch_bounds__(kScanThreads)
   }
 }
 
+// Largest R * nb for which every assign block derives its own offsets from
+// the per-block counts (otherwise a separate scan kernel computes them).
+constexpr int kFoldMax = 8192;
+
+// Slots of one block of tokens.  With fold == true this kernel also does the
+// scan: each block sums the per-block rank counts itself (its prefix within
+// each destination and the destinations' totals), and the blocks share out
+// the per-source totals and recv_base.  Otherwise the block offsets come from
+// layout_scan_kernel.
 __global__ void __launch_bounds__(kTok)
-    layout_assign_kernel(Geom g, Workspace ws, int32_t* __restrict__ slot) {
+    layout_assign_kernel(Geom g, Workspace ws, int32_t* __restrict__ slot, bool fold,
+                         int32_t* __restrict__ ntpr, int32_t* __restrict__ ntpe,
+                         int32_t* __restrict__ recv_base) {
   __shared__ int32_t warp_off[kTokWarps][EP_MAX_RANKS];
+  __shared__ int32_t blk_pre[EP_MAX_RANKS];
+  __shared__ int32_t tot[EP_MAX_RANKS];
+  __shared__ int32_t base[EP_MAX_RANKS + 1];
   const int b = blockIdx.x;
   const int s = b / g.nbps, c = b % g.nbps;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -222,6 +243,50 @@ __global__ void __launch_bounds__(kTok)
   const uint64_t mask = valid ? ws.masks[t] : 0;
   const unsigned lt = (1u << lane) - 1u;
 
+  if (fold) {
+    // per destination: the total over all blocks and the sum over blocks before b
+    for (int r = warp; r < g.R; r += kTokWarps) {
+      const int32_t* p = ws.blk_rank + (int64_t)r * g.nb;
+      int all = 0, pre = 0;
+#pragma unroll 4
+      for (int bb = lane; bb < g.nb; bb += 32) {
+        const int v = p[bb];
+        all += v;
+        pre += bb < b ? v : 0;
+      }
+      for (int o = 16; o > 0; o >>= 1) {
+        all += __shfl_xor_sync(0xFFFFFFFFu, all, o);
+        pre += __shfl_xor_sync(0xFFFFFFFFu, pre, o);
+      }
+      if (lane == 0) {
+        tot[r] = all;
+        blk_pre[r] = pre;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      base[0] = 0;
+      for (int r = 0; r < g.R; ++r) base[r + 1] = base[r] + tot[r];
+    }
+    __syncthreads();
+    // this block's share of the per-source totals and of recv_base
+    const int64_t n_rank = (int64_t)g.R * g.R, n_exp = (int64_t)g.R * g.E;
+    const int64_t n_out = n_rank + n_exp + g.R + 1;
+    for (int64_t i = (int64_t)b * kTok + threadIdx.x; i < n_out; i += (int64_t)g.nb * kTok) {
+      if (i < n_rank) {
+        const int so = (int)(i / g.R), r = (int)(i % g.R);
+        ntpr[i] = strided_sum(ws.blk_rank + (int64_t)r * g.nb + (int64_t)so * g.nbps, g.nbps, 1);
+      } else if (i < n_rank + n_exp) {
+        const int64_t k = i - n_rank;
+        const int so = (int)(k / g.E), e = (int)(k % g.E);
+        ntpe[k] = strided_sum(ws.blk_expert + (int64_t)so * g.nbps * g.E + e, g.nbps, g.E);
+      } else {
+        const int r = (int)(i - n_rank - n_exp);
+        recv_base[r] = base[r];
+      }
+    }
+  }
+
   for (int r = 0; r < g.R; ++r) {
     const unsigned bal = __ballot_sync(0xFFFFFFFFu, (mask >> r) & 1);
     if (lane == 0) warp_off[warp][r] = __popc(bal);
@@ -229,7 +294,7 @@ __global__ void __launch_bounds__(kTok)
   __syncthreads();
   if (threadIdx.x < g.R) {
     const int r = threadIdx.x;
-    int run = ws.blk_off[(int64_t)r * g.nb + b];
+    int run = fold ? base[r] + blk_pre[r] : ws.blk_off[(int64_t)r * g.nb + b];
     for (int w = 0; w < kTokWarps; ++w) {
       const int v = warp_off[w][r];
       warp_off[w][r] = run;
@@ -256,6 +321,20 @@ __global__ void __launch_bounds__(kTok)
       if (valid) dst[r] = in ? warp_off[warp][r] + __popc(bal & lt) : -1;
     }
   }
+}
+
+// The layout's launches on one stream, given carved scratch.
+void launch_layout(const int64_t* topk_idx, const Geom& g, const Workspace& ws,
+                   int32_t* ntpr, int32_t* ntpe, uint8_t* is_token_in_rank, int32_t* slot,
+                   int32_t* recv_base, int32_t* err_word, cudaStream_t st) {
+  if (g.nb > 0) {
+    const size_t smem = sizeof(int32_t) * ((size_t)g.E + (size_t)kTokWarps * g.R);
+    layout_count_kernel<<<g.nb, kTok, smem, st>>>(topk_idx, g, is_token_in_rank, ws, err_word);
+  }
+  const bool fold = g.nb > 0 && (int64_t)g.R * g.nb <= kFoldMax;
+  if (!fold) layout_scan_kernel<<<1, kScanThreads, 0, st>>>(g, ws, ntpr, ntpe, recv_base);
+  if (g.nb > 0)
+    layout_assign_kernel<<<g.nb, kTok, 0, st>>>(g, ws, slot, fold, ntpr, ntpe, recv_base);
 }
 
 }  // namespace
@@ -288,14 +367,8 @@ extern "C" ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t n
   const Geom g = make_geom(num_tokens, num_topk, num_experts, num_ranks);
   const Workspace ws = carve(g, workspace);
   if (num_tokens > 0 && workspace_bytes < ws.bytes) return EP_ERR_CAPACITY;
-  cudaStream_t st = to_cuda(stream);
-  if (g.nb > 0) {
-    const size_t smem = sizeof(int32_t) * ((size_t)g.E + (size_t)kTokWarps * g.R);
-    layout_count_kernel<<<g.nb, kTok, smem, st>>>(topk_idx, g, is_token_in_rank, ws, err_word);
-  }
-  layout_scan_kernel<<<1, kScanThreads, 0, st>>>(g, ws, num_tokens_per_rank,
-                                                 num_tokens_per_expert, recv_base);
-  if (g.nb > 0) layout_assign_kernel<<<g.nb, kTok, 0, st>>>(g, ws, slot);
+  launch_layout(topk_idx, g, ws, num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank,
+                slot, recv_base, err_word, to_cuda(stream));
   return launch_status();
 }
 
@@ -368,13 +441,7 @@ extern "C" ep_status_t ep_get_dispatch_layout_noalloc(
   const ep_status_t s = noalloc_scratch(&scratch);
   if (s != EP_OK) return s;
   const Workspace ws = carve(g, scratch);
-  cudaStream_t st = to_cuda(stream);
-  if (g.nb > 0) {
-    const size_t smem = sizeof(int32_t) * ((size_t)g.E + (size_t)kTokWarps * g.R);
-    layout_count_kernel<<<g.nb, kTok, smem, st>>>(topk_idx, g, is_token_in_rank, ws, err_word);
-  }
-  layout_scan_kernel<<<1, kScanThreads, 0, st>>>(g, ws, num_tokens_per_rank,
-                                                 num_tokens_per_expert, recv_base);
-  if (g.nb > 0) layout_assign_kernel<<<g.nb, kTok, 0, st>>>(g, ws, slot);
+  launch_layout(topk_idx, g, ws, num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank,
+                slot, recv_base, err_word, to_cuda(stream));
   return launch_status();
 }

@@ -8,7 +8,8 @@ synthetic routing and hidden states, on one GB300 per process.
 Prints one JSON line (rank 0).  `value` is whole-job tokens/s with inputs
 resident in HBM; `e2e` is the same metric with the step's inputs copied from
 pinned host memory and the combined output copied back inside the timed
-region (pipelined over token chunks on two copy streams).  Multi-GPU runs (torchrun) are independent replicas, one problem per
+region (pipelined over token chunks on two copy streams; consecutive steps
+overlap their copies, chunk by chunk).  Multi-GPU runs (torchrun) are independent replicas, one problem per
 GPU (the shuffle on one GPU has no cross-GPU step): per-GPU work is fixed,
 value = N * T / max-over-ranks step time.
 
@@ -374,19 +375,23 @@ def run_ours(args, cfg: Config):
     n_chunks = max(1, min(args.e2e_chunks, T // 8192))  # chunks of at least 8192 tokens
     bounds = [T * i // n_chunks for i in range(n_chunks + 1)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(n_chunks)]
-    ev_done = [torch.cuda.Event() for _ in range(n_chunks)]
-    ev_begin, ev_back = torch.cuda.Event(), torch.cuda.Event()
+    ev_in = [torch.cuda.Event() for _ in range(n_chunks)]      # x chunk landed
+    ev_used = [torch.cuda.Event() for _ in range(n_chunks)]    # x chunk read by dispatch
+    ev_done = [torch.cuda.Event() for _ in range(n_chunks)]    # out chunk computed
+    ev_back = [torch.cuda.Event() for _ in range(n_chunks)]    # out chunk copied back
     from dataclasses import replace as _replace
+    first = [True]
 
     def e2e_step():
-        ev_begin.record(stream)
+        # routing in and layout on the compute stream (after the previous
+        # step's kernels, which read idx and w)
         idx.copy_(h_idx, non_blocking=True)
         w.copy_(h_w, non_blocking=True)
-        s_in.wait_event(ev_begin)
         for c in range(n_chunks):
             a, b = bounds[c], bounds[c + 1]
             with torch.cuda.stream(s_in):
+                if not first[0]:
+                    s_in.wait_event(ev_used[c])  # the previous step has read this x chunk
                 x[a:b].copy_(h_x[a:b], non_blocking=True)
                 ev_in[c].record(s_in)
         ep.get_dispatch_layout(idx, E, R, err=err, out=L)
@@ -395,15 +400,23 @@ def run_ours(args, cfg: Config):
             stream.wait_event(ev_in[c])
             Lc = _replace(L, slot=L.slot[a:b], is_token_in_rank=L.is_token_in_rank[a:b])
             ep.dispatch(x[a:b], idx[a:b], w[a:b], Lc, use_fp8=cfg.fp8, err=err, out=D)
+            ev_used[c].record(stream)
+            if not first[0]:
+                stream.wait_event(ev_back[c])  # the previous step's copy of this out chunk is done
             ep.combine(Y, idx[a:b], w[a:b], Lc, err=err, out=out[a:b])
             ev_done[c].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_done[c])
                 h_out[a:b].copy_(out[a:b], non_blocking=True)
-        ev_back.record(s_out)
-        stream.wait_event(ev_back)
+                ev_back[c].record(s_out)
+        first[0] = False
+
+    def e2e_drain():
+        for c in range(n_chunks):
+            stream.wait_event(ev_back[c])
 
     e2e_step()
+    e2e_drain()
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
@@ -412,6 +425,7 @@ def run_ours(args, cfg: Config):
     e0.record(stream)
     for _ in range(e2e_steps):
         e2e_step()
+    e2e_drain()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)

@@ -217,16 +217,18 @@ def dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor
     return out
 
 
-def combine(y: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor,
+def combine(y: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor | None,
             layout: Layout, *, err: torch.Tensor | None = None,
             out: torch.Tensor | None = None) -> torch.Tensor:
     """out[t] = bf16(sum_k w[t][k] * y[slot[t][rank(e_k)]]) accumulated in
-    float32.  Enqueued on the current stream."""
+    float32; with topk_weights=None, the unweighted sum of the token's
+    destination-rank rows (each rank once).  Enqueued on the current stream."""
     _need(y, "y", torch.bfloat16)
     H = y.shape[1]
     T, K = topk_idx.shape
     _need(topk_idx, "topk_idx", torch.int64, (T, K))
-    _need(topk_weights, "topk_weights", torch.float32, (T, K))
+    if topk_weights is not None:
+        _need(topk_weights, "topk_weights", torch.float32, (T, K))
     R, E = layout.num_ranks, layout.num_experts
     _need(layout.slot, "slot", torch.int32, (T, R))
     if out is None:

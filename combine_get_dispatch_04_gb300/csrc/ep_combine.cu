@@ -7,6 +7,8 @@
 // shared memory tracked by an mbarrier, the "multi-source pull and reduce,
 // double buffered" pattern).  For every token t:
 //     out[t] = bf16_rne( sum_k w[t][k] * y[slot[t][rank(e_k)]] )   (float32)
+// or, without weights, the rank sum of DeepEP's high-throughput combine:
+//     out[t] = bf16_rne( sum over ranks r with slot[t][r] >= 0 of y[slot[t][r]] )
 //
 // Design: persistent CTAs, several per SM, three warp roles per CTA, all
 // communication through mbarriers in shared memory.
@@ -103,7 +105,7 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const 
 __device__ __forceinline__ int gather_token(const Args& a, int64_t t, int32_t* rows, float* W,
                                             bool& bad) {
   const int64_t* idx = a.topk_idx + t * a.K;
-  const float* wt = a.topk_w + t * a.K;
+  const float* wt = a.topk_w ? a.topk_w + t * a.K : nullptr;  // null: unweighted
   int D = 0;
   for (int k0 = 0; k0 < a.K; k0 += 8) {
     int64_t e[8];
@@ -112,7 +114,7 @@ __device__ __forceinline__ int gather_token(const Args& a, int64_t t, int32_t* r
     for (int u = 0; u < 8; ++u) {
       const int k = k0 + u;
       e[u] = k < a.K ? idx[k] : -1;
-      wv[u] = k < a.K ? wt[k] : 0.0f;
+      wv[u] = k < a.K ? (wt ? wt[k] : 1.0f) : 0.0f;
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -125,8 +127,8 @@ __device__ __forceinline__ int gather_token(const Args& a, int64_t t, int32_t* r
         if (jj < 0) {
           rows[D] = r;  // a rank for now; replaced by its row below
           W[D++] = wv[u];
-        } else {
-          W[jj] += wv[u];
+        } else if (wt) {
+          W[jj] += wv[u];  // unweighted: each rank's row counts once
         }
       } else if (e[u] != -1) {
         bad = true;
@@ -383,7 +385,7 @@ extern "C" ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk
   if (!routing_ok(num_tokens, num_topk, num_experts, num_ranks)) return EP_ERR_INVALID_ARG;
   if (hidden < 8 || hidden % 8 != 0) return EP_ERR_INVALID_ARG;
   if (num_tokens == 0) return EP_OK;
-  if (!y || !topk_idx || !topk_weights || !slot || !out) return EP_ERR_INVALID_ARG;
+  if (!y || !topk_idx || !slot || !out) return EP_ERR_INVALID_ARG;
   if (!aligned16(y) || !aligned16(out)) return EP_ERR_INVALID_ARG;
   DeviceProps props;
   if (!device_props(&props)) return EP_ERR_CUDA;

@@ -193,9 +193,14 @@ ep_status_t ep_dispatch(const void* x, int hidden, const int64_t* topk_idx,
  *                      w[t][k] * float(y[slot[t][rank(e_k)]]) )
  * accumulated in float32; a token whose slots are all masked gives +0.
  * A rank named by several slots contributes its row once per slot.
+ * With topk_weights == NULL the combine is the unweighted rank sum of the
+ * high-throughput kernels (the expert stage has applied the weights):
+ *   out[t] = bf16_rne( sum over ranks r with slot[t][r] >= 0 of y[slot[t][r]] ),
+ * each destination rank's row once.
  * In (device): y [rows, H] bf16 in dispatch's row layout (expert outputs,
  *   one row per (token, rank) pair); topk_idx [T, K] int64; topk_weights
- *   [T, K] float32; slot [T, R] int32 from ep_get_dispatch_layout.
+ *   [T, K] float32 (nullable, see above); slot [T, R] int32 from
+ *   ep_get_dispatch_layout.
  * Out (device): out [T, H] bf16, every element written.
  * err_word (device, nullable): EP_ERRBIT_BAD_EXPERT for ids outside [-1, E)
  *   (skipped), EP_ERRBIT_TIMEOUT if a bounded pipeline wait ran out (the

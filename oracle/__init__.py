@@ -30,6 +30,7 @@ def lib():
         L.oracle_dispatch.argtypes = [P, i64, i64, P, P, i32, i32, i32, P, i64, i64, i32,
                                       P, P, P, P, P]
         L.oracle_combine.argtypes = [P, i64, P, P, i64, i32, i32, i32, P, i64, i64, P]
+        L.oracle_combine_ranksum.argtypes = [P, i64, i64, i32, P, i64, i64, P]
         L.oracle_quantize_block_e4m3.argtypes = [P, i32, P, P]
         L.oracle_quantize_block_e4m3.restype = None
         for name in ("oracle_e4m3_from_float_n", "oracle_double_to_bf16_n",
@@ -37,7 +38,7 @@ def lib():
             getattr(L, name).argtypes = [P, i64, P]
             getattr(L, name).restype = None
         for name in ("oracle_layout", "oracle_num_recv_tokens_per_expert",
-                     "oracle_dispatch", "oracle_combine"):
+                     "oracle_dispatch", "oracle_combine", "oracle_combine_ranksum"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -148,6 +149,20 @@ def combine(y_bits: np.ndarray, topk_idx: np.ndarray, topk_weights: np.ndarray,
     _check(lib().oracle_combine(_p(y_bits), H, _p(topk_idx), _p(topk_weights), T, K,
                                 num_experts, num_ranks, _p(slot), t0, t1, _p(out)),
            "combine")
+    return out
+
+
+def combine_ranksum(y_bits: np.ndarray, slot: np.ndarray,
+                    t_range: tuple[int, int] | None = None) -> np.ndarray:
+    """Unweighted combine: each destination rank's row once; out [T, H] uint16."""
+    y_bits = np.ascontiguousarray(y_bits, dtype=np.uint16)
+    slot = np.ascontiguousarray(slot, dtype=np.int32)
+    H = y_bits.shape[1]
+    T, R = slot.shape
+    t0, t1 = t_range if t_range is not None else (0, T)
+    out = np.zeros((T, H), np.uint16)
+    _check(lib().oracle_combine_ranksum(_p(y_bits), H, T, R, _p(slot), t0, t1, _p(out)),
+           "combine_ranksum")
     return out
 
 

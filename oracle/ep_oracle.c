@@ -360,6 +360,34 @@ int oracle_combine(const uint16_t* y, int64_t H, const int64_t* topk_idx,
   return ORACLE_OK;
 }
 
+/*
+ * Unweighted rank-sum combine for tokens t in [t_begin, t_end) (DeepEP's
+ * high-throughput combine, where each receiving rank's expert stage has
+ * already applied the top-k weights and summed its local experts):
+ *   out[t][h] = bf16_rne( sum over ranks r with slot[t][r] >= 0 of y[slot[t][r]][h] )
+ * Each destination rank's row is added once, in rank order, in float64; a
+ * token sent nowhere gives +0.
+ */
+int oracle_combine_ranksum(const uint16_t* y, int64_t H, int64_t T, int R, const int32_t* slot,
+                           int64_t t_begin, int64_t t_end, uint16_t* out) {
+  if (T < 0 || H < 1 || R < 1) return ORACLE_BAD_ARG;
+  if (t_begin < 0 || t_end > T || t_begin > t_end) return ORACLE_BAD_ARG;
+  double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+  if (!acc) return ORACLE_NO_MEMORY;
+  for (int64_t t = t_begin; t < t_end; ++t) {
+    for (int64_t h = 0; h < H; ++h) acc[h] = 0.0;
+    for (int r = 0; r < R; ++r) {
+      int64_t p = slot[t * R + r];
+      if (p < 0) continue;
+      const uint16_t* row = y + p * H;
+      for (int64_t h = 0; h < H; ++h) acc[h] += oracle_bf16_to_double(row[h]);
+    }
+    for (int64_t h = 0; h < H; ++h) out[t * H + h] = oracle_double_to_bf16(acc[h]);
+  }
+  free(acc);
+  return ORACLE_OK;
+}
+
 /* Vector helpers so the number-format pins can sweep many values per call. */
 void oracle_e4m3_from_float_n(const float* x, int64_t n, uint8_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_from_float(x[i]);

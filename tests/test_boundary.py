@@ -96,7 +96,7 @@ def test_dispatch_rejects_bad_arguments(eplib):
 def test_combine_rejects_bad_arguments_and_accepts_empty(eplib):
     p = C.c_void_p(16)
     assert eplib.ep_combine(p, 12, p, p, 8, 2, 8, 2, p, p, None, None) == EP_ERR_INVALID_ARG
-    assert eplib.ep_combine(p, 256, p, None, 8, 2, 8, 2, p, p, None, None) == EP_ERR_INVALID_ARG
+    assert eplib.ep_combine(p, 256, None, p, 8, 2, 8, 2, p, p, None, None) == EP_ERR_INVALID_ARG
     assert eplib.ep_combine(C.c_void_p(8), 256, p, p, 8, 2, 8, 2, p, p, None, None) == EP_ERR_INVALID_ARG
     # no tokens: nothing to do, nothing enqueued
     assert eplib.ep_combine(None, 256, None, None, 0, 2, 8, 2, None, None, None, None) == 0

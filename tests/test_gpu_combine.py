@@ -161,3 +161,48 @@ def test_combine_full_size(ep, name):
             raise AssertionError(f"{bad.size} tokens differ (first {bad[:8].tolist()}); token {t}: "
                                  f"rows {rows} equal x: {same}; {ndiff} channels differ")
         assert not out2[~live].view(torch.int16).any()
+
+
+@pytest.mark.parametrize("cfg", small_configs()[:9] + [CONFIGS["tiny"]], ids=lambda c: c.name)
+def test_combine_unweighted_rank_sum(ep, cfg):
+    """topk_weights=None: each destination rank's row once (the high-throughput
+    combine's rank sum), against the oracle within the tolerance."""
+    c = make_case(cfg, with_hidden=False)
+    idx, _, _ = device_inputs(c)
+    L, P = layout_of(ep, cfg, idx)
+    y_bits = workloads.expert_outputs(max(P, 1), cfg.hidden, seed=cfg.seed + 3)
+    out = ep.combine(bf16_from_bits(y_bits), idx, None, L)
+    torch.cuda.synchronize()
+    slot = L.slot.cpu().numpy()
+    want = oracle.combine_ranksum(y_bits, slot)
+    yv = np.abs(oracle.bf16_to_double(y_bits))
+    bound = np.zeros((cfg.num_tokens, cfg.hidden))
+    for r in range(cfg.num_ranks):
+        p = slot[:, r]
+        bound[p >= 0] += yv[p[p >= 0]]
+    assert_combine_close(bits_of(out), want, bound)
+
+
+def test_combine_unweighted_full_skewed(ep):
+    """Rank sum at full size (skewed workload, dispatched rows as expert
+    outputs): sampled token ranges against the oracle."""
+    cfg = CONFIGS["skewed"]
+    c, want_layout = full_case("skewed")
+    idx, w, x = device_inputs(c)
+    L = ep.get_dispatch_layout(idx, cfg.num_experts, cfg.num_ranks)
+    d = ep.dispatch(x, idx, w, L)
+    out = ep.combine(d.recv_x, idx, None, L)
+    torch.cuda.synchronize()
+    slot = L.slot.cpu().numpy()
+    for (a, b) in sample_token_ranges(cfg.num_tokens):
+        toks = np.arange(a, b)
+        sub, orig, compact = compact_slots(slot, toks)
+        ysub = np.empty((orig.size, cfg.hidden), np.uint16)
+        ysub[compact] = bits_of(d.recv_x[torch.from_numpy(orig.astype(np.int64)).cuda()])
+        want = oracle.combine_ranksum(ysub, sub, t_range=(a, b))[a:b]
+        yv = np.abs(oracle.bf16_to_double(ysub))
+        bound = np.zeros((b - a, cfg.hidden))
+        for r in range(cfg.num_ranks):
+            p = sub[a:b, r]
+            bound[p >= 0] += yv[p[p >= 0]]
+        assert_combine_close(bits_of(out[a:b]), want, bound)

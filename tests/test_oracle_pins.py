@@ -481,3 +481,41 @@ def test_golden_tiny_layout():
     assert L.num_tokens_per_rank.ravel().tolist() == want["num_tokens_per_rank"]
     assert L.num_tokens_per_expert.ravel().tolist() == want["num_tokens_per_expert"]
     assert L.slot[:8].ravel().tolist() == want["slot_first_8_tokens"]
+
+
+def test_combine_ranksum_brute_force_exact_rounding():
+    """Unweighted combine (each destination rank's row once): exact rounding of
+    the exact sum, on a case with duplicate ranks per token and masked slots."""
+    cfg = Config("rsum", 3, 5, 16, 6, 4, routing="zipf", zipf_s=1.2, mask_prob=0.25, seed=41)
+    c = make_case(cfg)
+    L = oracle.layout(c.topk_idx, 6, 3)
+    y = workloads.expert_outputs(L.num_rows, 16, seed=42)
+    out = oracle.combine_ranksum(y, L.slot)
+    yv = oracle.bf16_to_double(y)
+    for t in range(cfg.num_tokens):
+        rows = [int(p) for p in L.slot[t] if p >= 0]
+        for h in range(16):
+            if not rows:
+                assert out[t, h] == 0
+            else:
+                _exact_bf16_check(out[t, h], [(1.0, float(yv[p, h])) for p in rows])
+
+
+def test_combine_ranksum_equals_weighted_with_one_weight_per_rank():
+    """Rank-sum equals the weighted combine when each rank's first slot has
+    weight 1 and its other slots weight 0 (a closed-form special case)."""
+    cfg = CONFIGS["tiny"]
+    c = make_case(cfg, with_hidden=False)
+    E, R = cfg.num_experts, cfg.num_ranks
+    L = oracle.layout(c.topk_idx, E, R)
+    y = workloads.expert_outputs(L.num_rows, cfg.hidden, seed=43)
+    w = np.zeros_like(c.topk_weights)
+    for t in range(cfg.num_tokens):
+        seen = set()
+        for k in range(cfg.num_topk):
+            r = c.topk_idx[t, k] // (E // R)
+            if c.topk_idx[t, k] >= 0 and r not in seen:
+                w[t, k] = 1.0
+                seen.add(r)
+    assert np.array_equal(oracle.combine_ranksum(y, L.slot),
+                          oracle.combine(y, c.topk_idx, w, E, R, L.slot))

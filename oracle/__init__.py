@@ -31,6 +31,9 @@ def lib():
                                       P, P, P, P, P]
         L.oracle_combine.argtypes = [P, i64, P, P, i64, i32, i32, i32, P, i64, i64, P]
         L.oracle_combine_ranksum.argtypes = [P, i64, i64, i32, P, i64, i64, P]
+        L.oracle_ll_layout.argtypes = [P, i64, i32, i32, i32, i64, P, P, P, P]
+        L.oracle_ll_dispatch.argtypes = [P, i64, i64, i32, P, i64, i64, i32, P, P, P]
+        L.oracle_ll_combine.argtypes = [P, i64, P, i64, i32, P, i64, i64, P]
         L.oracle_quantize_block_e4m3.argtypes = [P, i32, P, P]
         L.oracle_quantize_block_e4m3.restype = None
         for name in ("oracle_e4m3_from_float_n", "oracle_double_to_bf16_n",
@@ -38,7 +41,8 @@ def lib():
             getattr(L, name).argtypes = [P, i64, P]
             getattr(L, name).restype = None
         for name in ("oracle_layout", "oracle_num_recv_tokens_per_expert",
-                     "oracle_dispatch", "oracle_combine", "oracle_combine_ranksum"):
+                     "oracle_dispatch", "oracle_combine", "oracle_combine_ranksum",
+                     "oracle_ll_layout", "oracle_ll_dispatch", "oracle_ll_combine"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -163,6 +167,58 @@ def combine_ranksum(y_bits: np.ndarray, slot: np.ndarray,
     out = np.zeros((T, H), np.uint16)
     _check(lib().oracle_combine_ranksum(_p(y_bits), H, T, R, _p(slot), t0, t1, _p(out)),
            "combine_ranksum")
+    return out
+
+
+@dataclass
+class LLLayout:
+    ll_slot: np.ndarray        # [T, K] int32: row in the expert-major buffer, -1 = none
+    ll_count: np.ndarray       # [E] int32: rows each expert receives
+    ll_src_offset: np.ndarray  # [E, R] int32: first row of each source within its expert
+    err_bits: int
+
+
+def ll_layout(topk_idx: np.ndarray, num_experts: int, num_ranks: int,
+              expert_capacity: int) -> LLLayout:
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    T, K = topk_idx.shape
+    E, R = num_experts, num_ranks
+    slot = np.empty((T, K), np.int32)
+    cnt = np.empty(E, np.int32)
+    off = np.empty((E, R), np.int32)
+    err = np.zeros(1, np.int32)
+    _check(lib().oracle_ll_layout(_p(topk_idx), T, K, E, R, expert_capacity, _p(slot), _p(cnt),
+                                  _p(off), _p(err)), "ll_layout")
+    return LLLayout(slot, cnt, off, int(err[0]))
+
+
+def ll_dispatch(x_bits: np.ndarray, ll_slot: np.ndarray, num_rows: int, use_fp8: bool = False,
+                t_range: tuple[int, int] | None = None):
+    """(recv_x, recv_scales or None, recv_src_idx) over num_rows rows; untouched rows are 0 / -2."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    ll_slot = np.ascontiguousarray(ll_slot, dtype=np.int32)
+    T, H = x_bits.shape
+    K = ll_slot.shape[1]
+    t0, t1 = t_range if t_range is not None else (0, T)
+    recv = np.zeros((num_rows, H), np.uint8 if use_fp8 else np.uint16)
+    scales = np.zeros((num_rows, H // 128), np.float32) if use_fp8 else None
+    src = np.full(num_rows, -2, np.int32)
+    _check(lib().oracle_ll_dispatch(_p(x_bits), T, H, K, _p(ll_slot), t0, t1, int(use_fp8),
+                                    _p(recv), _p(scales), _p(src)), "ll_dispatch")
+    return recv, scales, src
+
+
+def ll_combine(y_bits: np.ndarray, topk_weights: np.ndarray | None, ll_slot: np.ndarray,
+               t_range: tuple[int, int] | None = None) -> np.ndarray:
+    y_bits = np.ascontiguousarray(y_bits, dtype=np.uint16)
+    ll_slot = np.ascontiguousarray(ll_slot, dtype=np.int32)
+    w = None if topk_weights is None else np.ascontiguousarray(topk_weights, dtype=np.float32)
+    H = y_bits.shape[1]
+    T, K = ll_slot.shape
+    t0, t1 = t_range if t_range is not None else (0, T)
+    out = np.zeros((T, H), np.uint16)
+    _check(lib().oracle_ll_combine(_p(y_bits), H, _p(w), T, K, _p(ll_slot), t0, t1, _p(out)),
+           "ll_combine")
     return out
 
 

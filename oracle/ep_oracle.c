@@ -388,6 +388,145 @@ int oracle_combine_ranksum(const uint16_t* y, int64_t H, int64_t T, int R, const
   return ORACLE_OK;
 }
 
+/* ---------------------------------------------------------------------- */
+/* low-latency (expert-major) layout                                        */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * The low-latency kernels' receive layout ("[Not ready] MSCCLPP EP
+ * implementation", the low-latency port: dispatch<kUseFP8,...> and combine
+ * address per-expert buffers, [local_expert * num_ranks + dst_rank]): every
+ * unmasked top-k slot (t, k) gets its own row in the buffer of expert
+ * e = topk_idx[t][k].  Expert e owns rows [e*cap, (e+1)*cap); inside it the
+ * rows are packed by source rank, then by token, then by k:
+ *   ll_slot[t][k]       = e*cap + ll_src_offset[e][src(t)]
+ *                         + #{(t', k') of src(t) before (t, k), topk_idx[t'][k'] == e}
+ *   ll_count[e]         = slots naming e (over all sources)
+ *   ll_src_offset[e][s] = slots naming e from sources before s
+ * Masked slots and ids outside [0, E) get -1 (the latter set the error bit);
+ * a slot whose position is >= cap gets -1 and sets ORACLE_ERR_CAPACITY.
+ */
+#define ORACLE_ERR_CAPACITY 2
+int oracle_ll_layout(const int64_t* topk_idx, int64_t T, int K, int E, int R, int64_t cap,
+                     int32_t* ll_slot, int32_t* ll_count, int32_t* ll_src_offset,
+                     int32_t* err_bits) {
+  if (T < 0 || K < 1 || E < 1 || R < 1 || E % R || T % R || cap < 0) return ORACLE_BAD_ARG;
+  const int64_t Tr = T / R;
+  *err_bits = 0;
+  int64_t* per_src = (int64_t*)calloc((size_t)E * R, sizeof(int64_t));  /* [e][s] */
+  int64_t* seen = (int64_t*)calloc((size_t)E * R, sizeof(int64_t));
+  if (!per_src || !seen) {
+    free(per_src);
+    free(seen);
+    return ORACLE_NO_MEMORY;
+  }
+  for (int64_t t = 0; t < T; ++t)
+    for (int k = 0; k < K; ++k) {
+      int64_t e = topk_idx[t * K + k];
+      if (e == -1) continue;
+      if (e < -1 || e >= E) {
+        *err_bits |= ORACLE_ERR_BAD_EXPERT;
+        continue;
+      }
+      per_src[e * R + t / Tr] += 1;
+    }
+  for (int e = 0; e < E; ++e) {
+    int64_t run = 0;
+    for (int s = 0; s < R; ++s) {
+      ll_src_offset[e * R + s] = (int32_t)run;
+      run += per_src[e * R + s];
+    }
+    ll_count[e] = (int32_t)run;
+  }
+  for (int64_t t = 0; t < T; ++t) {
+    const int64_t s = t / Tr;
+    for (int k = 0; k < K; ++k) {
+      int64_t e = topk_idx[t * K + k];
+      if (e < 0 || e >= E) {
+        ll_slot[t * K + k] = -1;
+        continue;
+      }
+      int64_t pos = ll_src_offset[e * R + s] + seen[e * R + s];
+      seen[e * R + s] += 1;
+      if (pos >= cap) {
+        ll_slot[t * K + k] = -1;
+        *err_bits |= ORACLE_ERR_CAPACITY;
+      } else {
+        ll_slot[t * K + k] = (int32_t)(e * cap + pos);
+      }
+    }
+  }
+  free(per_src);
+  free(seen);
+  return ORACLE_OK;
+}
+
+/* Low-latency dispatch of tokens in [t_begin, t_end): recv_x[ll_slot[t][k]]
+   = x[t] (bf16) or its E4M3 codes with recv_scales (per 128 channels, as in
+   oracle_dispatch), recv_src_idx[ll_slot[t][k]] = t, for every slot >= 0. */
+int oracle_ll_dispatch(const uint16_t* x, int64_t T, int64_t H, int K, const int32_t* ll_slot,
+                       int64_t t_begin, int64_t t_end, int use_fp8, void* recv_x,
+                       float* recv_scales, int32_t* recv_src_idx) {
+  if (T < 0 || H < 1 || K < 1) return ORACLE_BAD_ARG;
+  if (t_begin < 0 || t_end > T || t_begin > t_end) return ORACLE_BAD_ARG;
+  if (use_fp8 && H % 128) return ORACLE_BAD_ARG;
+  const int64_t nb = H / 128;
+  uint8_t* q = NULL;
+  float* scales = NULL;
+  if (use_fp8) {
+    q = (uint8_t*)malloc((size_t)H);
+    scales = (float*)malloc(sizeof(float) * (size_t)(nb ? nb : 1));
+    if (!q || !scales) {
+      free(q);
+      free(scales);
+      return ORACLE_NO_MEMORY;
+    }
+  }
+  for (int64_t t = t_begin; t < t_end; ++t) {
+    const uint16_t* row = x + t * H;
+    if (use_fp8)
+      for (int64_t b = 0; b < nb; ++b) oracle_quantize_block_e4m3(row + b * 128, 128, q + b * 128, scales + b);
+    for (int k = 0; k < K; ++k) {
+      int64_t p = ll_slot[t * K + k];
+      if (p < 0) continue;
+      if (use_fp8) {
+        memcpy((uint8_t*)recv_x + p * H, q, (size_t)H);
+        memcpy(recv_scales + p * nb, scales, sizeof(float) * (size_t)nb);
+      } else {
+        memcpy((uint16_t*)recv_x + p * H, row, sizeof(uint16_t) * (size_t)H);
+      }
+      if (recv_src_idx) recv_src_idx[p] = (int32_t)t;
+    }
+  }
+  free(q);
+  free(scales);
+  return ORACLE_OK;
+}
+
+/* Low-latency combine of tokens in [t_begin, t_end): out[t] = bf16_rne( sum
+   over slots k with ll_slot[t][k] >= 0 of w[t][k] * y[ll_slot[t][k]] ), in
+   float64, k ascending; with w == NULL every slot weighs 1. */
+int oracle_ll_combine(const uint16_t* y, int64_t H, const float* w, int64_t T, int K,
+                      const int32_t* ll_slot, int64_t t_begin, int64_t t_end, uint16_t* out) {
+  if (T < 0 || H < 1 || K < 1) return ORACLE_BAD_ARG;
+  if (t_begin < 0 || t_end > T || t_begin > t_end) return ORACLE_BAD_ARG;
+  double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+  if (!acc) return ORACLE_NO_MEMORY;
+  for (int64_t t = t_begin; t < t_end; ++t) {
+    for (int64_t h = 0; h < H; ++h) acc[h] = 0.0;
+    for (int k = 0; k < K; ++k) {
+      int64_t p = ll_slot[t * K + k];
+      if (p < 0) continue;
+      double wk = w ? (double)w[t * K + k] : 1.0;
+      const uint16_t* row = y + p * H;
+      for (int64_t h = 0; h < H; ++h) acc[h] += wk * oracle_bf16_to_double(row[h]);
+    }
+    for (int64_t h = 0; h < H; ++h) out[t * H + h] = oracle_double_to_bf16(acc[h]);
+  }
+  free(acc);
+  return ORACLE_OK;
+}
+
 /* Vector helpers so the number-format pins can sweep many values per call. */
 void oracle_e4m3_from_float_n(const float* x, int64_t n, uint8_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_from_float(x[i]);

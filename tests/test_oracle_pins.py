@@ -519,3 +519,142 @@ def test_combine_ranksum_equals_weighted_with_one_weight_per_rank():
                 seen.add(r)
     assert np.array_equal(oracle.combine_ranksum(y, L.slot),
                           oracle.combine(y, c.topk_idx, w, E, R, L.slot))
+
+
+# --------------------------------------------------------------------------
+# low-latency (expert-major) layout, dispatch and combine
+# --------------------------------------------------------------------------
+def brute_ll_layout(topk_idx, E, R, cap):
+    """Walk experts, then source ranks, then tokens, then k, handing out rows."""
+    T, K = topk_idx.shape
+    Tr = T // R
+    slot = np.full((T, K), -1, np.int32)
+    count = np.zeros(E, np.int32)
+    off = np.zeros((E, R), np.int32)
+    bad = 0
+    for e in range(E):
+        pos = 0
+        for s in range(R):
+            off[e, s] = pos
+            for t in range(s * Tr, (s + 1) * Tr):
+                for k in range(K):
+                    if topk_idx[t, k] == e:
+                        if pos < cap:
+                            slot[t, k] = e * cap + pos
+                        else:
+                            bad |= 2
+                        pos += 1
+        count[e] = pos
+    if ((topk_idx < -1) | (topk_idx >= E)).any():
+        bad |= 1
+    return slot, count, off, bad
+
+
+LL_CASES = [Config("ll0", 4, 32, 16, 16, 4, seed=61), Config("ll1", 3, 7, 8, 9, 2, routing="zipf",
+            zipf_s=1.2, mask_prob=0.2, seed=62), Config("ll2", 8, 5, 8, 64, 8, seed=63),
+            Config("ll3", 1, 40, 8, 5, 3, routing="zipf", zipf_s=1.2, seed=64)]
+
+
+@pytest.mark.parametrize("cfg", LL_CASES, ids=lambda c: c.name)
+def test_ll_layout_matches_brute_force_and_ht_counts(cfg):
+    c = make_case(cfg, with_hidden=False)
+    E, R, T = cfg.num_experts, cfg.num_ranks, cfg.num_tokens
+    got = oracle.ll_layout(c.topk_idx, E, R, T)
+    slot, count, off, bad = brute_ll_layout(c.topk_idx, E, R, T)
+    np.testing.assert_array_equal(got.ll_slot, slot)
+    np.testing.assert_array_equal(got.ll_count, count)
+    np.testing.assert_array_equal(got.ll_src_offset, off)
+    assert got.err_bits == bad == 0
+    # per-expert counts are the column sums of the high-throughput layout's
+    # per-source expert counts, and each expert's rows are a bijection onto
+    # [e*cap, e*cap + count)
+    ht = oracle.layout(c.topk_idx, E, R)
+    np.testing.assert_array_equal(got.ll_count, ht.num_tokens_per_expert.sum(axis=0))
+    for e in range(E):
+        rows = np.sort(got.ll_slot[c.topk_idx == e])
+        assert np.array_equal(rows, e * T + np.arange(got.ll_count[e]))
+
+
+def test_ll_layout_duplicates_and_capacity():
+    idx = np.array([[2, 2, 0], [1, 2, -1], [2, 0, 2], [-1, -1, -1]], np.int64)
+    got = oracle.ll_layout(idx, 3, 1, 3)
+    slot, count, off, bad = brute_ll_layout(idx, 3, 1, 3)
+    np.testing.assert_array_equal(got.ll_slot, slot)
+    np.testing.assert_array_equal(got.ll_count, count)
+    assert got.ll_count.tolist() == [2, 1, 5] and got.err_bits == bad == 2
+    # expert 2 rows in (token, k) order: (0,0) (0,1) (1,1) then capacity
+    assert got.ll_slot[0].tolist() == [6, 7, 0] and got.ll_slot[1].tolist() == [3, 8, -1]
+    assert got.ll_slot[2].tolist() == [-1, 1, -1]
+
+
+@pytest.mark.parametrize("use_fp8", [False, True])
+def test_ll_dispatch_brute_force(use_fp8):
+    cfg = Config("lld", 2, 6, 256, 8, 3, seed=65)
+    c = make_case(cfg)
+    E, R, T = 8, 2, cfg.num_tokens
+    L = oracle.ll_layout(c.topk_idx, E, R, T)
+    recv, scales, src = oracle.ll_dispatch(c.x_bits, L.ll_slot, E * T, use_fp8=use_fp8)
+    for t in range(T):
+        for k in range(3):
+            p = L.ll_slot[t, k]
+            if p < 0:
+                continue
+            assert src[p] == t
+            if use_fp8:
+                for b in range(2):
+                    qt, st = torch_quantize_block(c.x_bits[t, b * 128:(b + 1) * 128])
+                    assert np.array_equal(recv[p, b * 128:(b + 1) * 128], qt)
+                    assert scales[p, b] == np.float32(st)
+            else:
+                assert np.array_equal(recv[p], c.x_bits[t])
+    assert (src >= 0).sum() == (L.ll_slot >= 0).sum()
+
+
+def test_ll_combine_equals_ht_combine_on_copied_rows():
+    """With every expert row a copy of its rank's row, the expert-major combine
+    has the same terms, in the same k order, as the rank-major one: equal bits."""
+    cfg = Config("llc", 4, 16, 24, 16, 4, routing="zipf", zipf_s=1.2, mask_prob=0.1, seed=66)
+    c = make_case(cfg, with_hidden=False)
+    E, R, T, K = 16, 4, cfg.num_tokens, 4
+    ht = oracle.layout(c.topk_idx, E, R)
+    ll = oracle.ll_layout(c.topk_idx, E, R, T)
+    y_ht = workloads.expert_outputs(ht.num_rows, 24, seed=67)
+    y_ll = np.zeros((E * T, 24), np.uint16)
+    for t in range(T):
+        for k in range(K):
+            e = c.topk_idx[t, k]
+            if e >= 0:
+                y_ll[ll.ll_slot[t, k]] = y_ht[ht.slot[t, e // (E // R)]]
+    w = workloads.random_weights(np.random.default_rng(68), T, K)
+    assert np.array_equal(oracle.ll_combine(y_ll, w, ll.ll_slot),
+                          oracle.combine(y_ht, c.topk_idx, w, E, R, ht.slot))
+
+
+def test_ll_combine_brute_force_exact_rounding():
+    cfg = Config("llx", 2, 6, 8, 6, 3, mask_prob=0.2, seed=69)
+    c = make_case(cfg, with_hidden=False)
+    L = oracle.ll_layout(c.topk_idx, 6, 2, cfg.num_tokens)
+    y = workloads.expert_outputs(6 * cfg.num_tokens, 8, seed=70)
+    yv = oracle.bf16_to_double(y)
+    for w in (c.topk_weights, None):
+        out = oracle.ll_combine(y, w, L.ll_slot)
+        for t in range(cfg.num_tokens):
+            terms = [(1.0 if w is None else float(w[t, k]), None, L.ll_slot[t, k])
+                     for k in range(3) if L.ll_slot[t, k] >= 0]
+            for h in range(8):
+                if not terms:
+                    assert out[t, h] == 0
+                else:
+                    _exact_bf16_check(out[t, h], [(wk, float(yv[p, h])) for wk, _, p in terms])
+
+
+def test_ll_round_trip_identity_experts():
+    cfg = CONFIGS["decode_fp8"].scaled(8)
+    c = make_case(cfg)
+    E, R, T = cfg.num_experts, cfg.num_ranks, cfg.num_tokens
+    L = oracle.ll_layout(c.topk_idx, E, R, T)
+    recv, _, _ = oracle.ll_dispatch(c.x_bits, L.ll_slot, E * T)
+    w = c.topk_weights.astype(np.float64)
+    w = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+    out = oracle.ll_combine(recv, w, L.ll_slot)
+    assert np.array_equal(oracle.bf16_to_double(out), oracle.bf16_to_double(c.x_bits))

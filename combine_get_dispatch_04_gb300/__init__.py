@@ -34,7 +34,8 @@ EP_MAX_EXPERTS = 4096
 # every entry point declared in include/ep.h
 EXPORTED = ("ep_status_string", "ep_workspace_bytes", "ep_get_dispatch_layout",
             "ep_get_dispatch_layout_noalloc", "ep_layout_total_rows", "ep_dispatch",
-            "ep_combine")
+            "ep_combine", "ep_ll_workspace_bytes", "ep_ll_get_dispatch_layout",
+            "ep_ll_dispatch", "ep_ll_combine")
 
 _lib = None
 
@@ -63,7 +64,13 @@ def load(path: str | None = None) -> C.CDLL:
     L.ep_dispatch.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, i64, i32, P, P, P, P, P,
                               P, P, P]
     L.ep_combine.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, P, P]
-    for name in ("ep_get_dispatch_layout", "ep_layout_total_rows", "ep_dispatch", "ep_combine"):
+    L.ep_ll_workspace_bytes.argtypes = [i64, i32, i32]
+    L.ep_ll_workspace_bytes.restype = sz
+    L.ep_ll_get_dispatch_layout.argtypes = [P, i64, i32, i32, i32, i64, P, P, P, P, P, sz, P]
+    L.ep_ll_dispatch.argtypes = [P, i32, i64, i32, P, i64, i32, P, P, P, P, P]
+    L.ep_ll_combine.argtypes = [P, i32, P, i64, i32, P, P, P, P]
+    for name in ("ep_get_dispatch_layout", "ep_layout_total_rows", "ep_dispatch", "ep_combine",
+                 "ep_ll_get_dispatch_layout", "ep_ll_dispatch", "ep_ll_combine"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -239,4 +246,94 @@ def combine(y: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor 
     _check(lib().ep_combine(_ptr(y), H, _ptr(topk_idx), _ptr(topk_weights), T, K, E, R,
                             _ptr(layout.slot), _ptr(out), _ptr(err), _stream(y.device)),
            "ep_combine")
+    return out
+
+
+# --------------------------------------------------------------------------
+# low-latency (expert-major) layout
+# --------------------------------------------------------------------------
+@dataclass
+class LLLayout:
+    """Outputs of ll_get_dispatch_layout (all on the device)."""
+    ll_slot: torch.Tensor        # [T, K] int32: row of each slot, -1 = none
+    ll_count: torch.Tensor       # [E] int32: rows each expert receives
+    ll_src_offset: torch.Tensor  # [E, R] int32: first row of each source within its expert
+    num_experts: int
+    num_ranks: int
+    expert_capacity: int
+    workspace: torch.Tensor | None = None
+
+    @property
+    def num_rows(self) -> int:
+        """Rows of the expert-major buffer: E * expert_capacity."""
+        return self.num_experts * self.expert_capacity
+
+
+def ll_get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int,
+                           expert_capacity: int | None = None, *,
+                           err: torch.Tensor | None = None) -> LLLayout:
+    """Rows of the expert-major layout (default capacity: T rows per expert)."""
+    _need(topk_idx, "topk_idx", torch.int64)
+    T, K = topk_idx.shape
+    cap = T if expert_capacity is None else int(expert_capacity)
+    dev = topk_idx.device
+    ws = torch.empty(max(int(lib().ep_ll_workspace_bytes(T, num_ranks, num_experts)), 16),
+                     dtype=torch.uint8, device=dev)
+    L = LLLayout(torch.empty((T, K), dtype=torch.int32, device=dev),
+                 torch.empty(num_experts, dtype=torch.int32, device=dev),
+                 torch.empty((num_experts, num_ranks), dtype=torch.int32, device=dev),
+                 num_experts, num_ranks, cap, ws)
+    if err is not None:
+        _need(err, "err", torch.int32)
+    _check(lib().ep_ll_get_dispatch_layout(
+        _ptr(topk_idx), T, K, num_experts, num_ranks, cap, _ptr(L.ll_slot), _ptr(L.ll_count),
+        _ptr(L.ll_src_offset), _ptr(err), _ptr(ws), ws.numel(), _stream(dev)),
+        "ep_ll_get_dispatch_layout")
+    return L
+
+
+@dataclass
+class LLDispatched:
+    recv_x: torch.Tensor              # [E*cap, H] bf16 or uint8 (E4M3)
+    recv_scales: torch.Tensor | None  # [E*cap, H/128] float32 (FP8 only)
+    recv_src_idx: torch.Tensor        # [E*cap] int32
+    use_fp8: bool
+
+
+def ll_dispatch(x: torch.Tensor, layout: LLLayout, *, use_fp8: bool = False,
+                err: torch.Tensor | None = None, out: LLDispatched | None = None) -> LLDispatched:
+    _need(x, "x", torch.bfloat16)
+    T, H = x.shape
+    K = layout.ll_slot.shape[1]
+    _need(layout.ll_slot, "ll_slot", torch.int32, (T, K))
+    rows = layout.num_rows
+    if out is None:
+        dev = x.device
+        out = LLDispatched(
+            torch.empty((rows, H), dtype=torch.uint8 if use_fp8 else torch.bfloat16, device=dev),
+            torch.empty((rows, H // 128), dtype=torch.float32, device=dev) if use_fp8 else None,
+            torch.empty(rows, dtype=torch.int32, device=dev), use_fp8)
+    if err is not None:
+        _need(err, "err", torch.int32)
+    _check(lib().ep_ll_dispatch(_ptr(x), H, T, K, _ptr(layout.ll_slot), out.recv_x.shape[0],
+                                int(use_fp8), _ptr(out.recv_x), _ptr(out.recv_scales),
+                                _ptr(out.recv_src_idx), _ptr(err), _stream(x.device)),
+           "ep_ll_dispatch")
+    return out
+
+
+def ll_combine(y: torch.Tensor, topk_weights: torch.Tensor | None, layout: LLLayout, *,
+               err: torch.Tensor | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
+    _need(y, "y", torch.bfloat16)
+    H = y.shape[1]
+    T, K = layout.ll_slot.shape
+    if topk_weights is not None:
+        _need(topk_weights, "topk_weights", torch.float32, (T, K))
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device)
+    _need(out, "out", torch.bfloat16, (T, H))
+    if err is not None:
+        _need(err, "err", torch.int32)
+    _check(lib().ep_ll_combine(_ptr(y), H, _ptr(topk_weights), T, K, _ptr(layout.ll_slot),
+                               _ptr(out), _ptr(err), _stream(y.device)), "ep_ll_combine")
     return out

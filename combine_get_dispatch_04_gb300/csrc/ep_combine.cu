@@ -61,6 +61,7 @@ struct Args {
   const float* topk_w;
   int K, E, El, R;
   const int32_t* slot;
+  const int32_t* ll_slot;  // non-null: expert-major rows, one per top-k slot
   int32_t* err;
   int C;       // channels per chunk (multiple of 8)
   int nchunk;  // chunks per token
@@ -104,9 +105,30 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const 
 // rank.  Global loads are issued eight slots at a time before any is used.
 __device__ __forceinline__ int gather_token(const Args& a, int64_t t, int32_t* rows, float* W,
                                             bool& bad) {
-  const int64_t* idx = a.topk_idx + t * a.K;
   const float* wt = a.topk_w ? a.topk_w + t * a.K : nullptr;  // null: unweighted
   int D = 0;
+  if (a.ll_slot) {  // expert-major: each live slot has its own row
+    const int32_t* ls = a.ll_slot + t * a.K;
+    for (int k0 = 0; k0 < a.K; k0 += 8) {
+      int32_t p[8];
+      float wv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u;
+        p[u] = k < a.K ? ls[k] : -1;
+        wv[u] = k < a.K ? (wt ? wt[k] : 1.0f) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (p[u] >= 0) {
+          rows[D] = p[u];
+          W[D++] = wv[u];
+        }
+      }
+    }
+    return D;
+  }
+  const int64_t* idx = a.topk_idx + t * a.K;
   for (int k0 = 0; k0 < a.K; k0 += 8) {
     int64_t e[8];
     float wv[8];
@@ -374,6 +396,33 @@ bool make_plan(int H, int K, int R, const DeviceProps& p, Plan* out) {
 }
 
 }  // namespace
+
+// Plan, occupancy-sized persistent grid and launch, shared by the rank-major
+// and expert-major combine.
+ep_status_t launch_combine(Args& a, const DeviceProps& props, ep_stream_t stream) {
+  Plan plan;
+  if (!make_plan(a.H, a.dmax, a.dmax, props, &plan)) return EP_ERR_INVALID_ARG;
+  a.C = plan.C;
+  a.S = plan.S;
+  a.stage_bytes = plan.stage_bytes;
+  a.nchunk = (a.H + a.C - 1) / a.C;
+  // rows per token <= 8 (every workload here): unrolled reduction
+  void (*kernel)(Args) = a.dmax <= 8 ? combine_kernel<8> : combine_kernel<0>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)plan.smem) != cudaSuccess)
+    return EP_ERR_CUDA;
+  int resident = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, kThreads, plan.smem) !=
+      cudaSuccess)
+    return EP_ERR_CUDA;
+  if (resident < 1) return EP_ERR_CUDA;
+  const int64_t ctas =
+      (int64_t)props.sm_count * (resident < plan.ctas_per_sm ? resident : plan.ctas_per_sm);
+  const int64_t grid = a.T < ctas ? a.T : ctas;
+  kernel<<<(unsigned)grid, kThreads, plan.smem, to_cuda(stream)>>>(a);
+  return launch_status();
+}
+
 }  // namespace ep
 
 using namespace ep;
@@ -389,9 +438,7 @@ extern "C" ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk
   if (!aligned16(y) || !aligned16(out)) return EP_ERR_INVALID_ARG;
   DeviceProps props;
   if (!device_props(&props)) return EP_ERR_CUDA;
-  Plan plan;
-  if (!make_plan(hidden, num_topk, num_ranks, props, &plan)) return EP_ERR_INVALID_ARG;
-  Args a;
+  Args a = {};
   a.y = static_cast<const uint16_t*>(y);
   a.out = static_cast<uint16_t*>(out);
   a.T = num_tokens;
@@ -403,24 +450,31 @@ extern "C" ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk
   a.El = num_experts / num_ranks;
   a.R = num_ranks;
   a.slot = slot;
+  a.ll_slot = nullptr;
   a.err = err_word;
   a.dmax = num_topk < num_ranks ? num_topk : num_ranks;
-  a.C = plan.C;
-  a.S = plan.S;
-  a.stage_bytes = plan.stage_bytes;
-  a.nchunk = (hidden + a.C - 1) / a.C;
-  // rows per token <= 8 (every workload here): unrolled reduction
-  void (*kernel)(Args) = a.dmax <= 8 ? combine_kernel<8> : combine_kernel<0>;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)plan.smem) != cudaSuccess)
-    return EP_ERR_CUDA;
-  int resident = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, kThreads, plan.smem) !=
-      cudaSuccess)
-    return EP_ERR_CUDA;
-  if (resident < 1) return EP_ERR_CUDA;
-  const int64_t ctas = (int64_t)props.sm_count * (resident < plan.ctas_per_sm ? resident : plan.ctas_per_sm);
-  const int64_t grid = num_tokens < ctas ? num_tokens : ctas;
-  kernel<<<(unsigned)grid, kThreads, plan.smem, to_cuda(stream)>>>(a);
-  return launch_status();
+  return launch_combine(a, props, stream);
+}
+
+extern "C" ep_status_t ep_ll_combine(const void* y, int hidden, const float* topk_weights,
+                                     int64_t num_tokens, int num_topk, const int32_t* ll_slot,
+                                     void* out, int32_t* err_word, ep_stream_t stream) {
+  if (num_tokens < 0 || num_topk < 1 || num_topk > EP_MAX_TOPK) return EP_ERR_INVALID_ARG;
+  if (hidden < 8 || hidden % 8 != 0) return EP_ERR_INVALID_ARG;
+  if (num_tokens == 0) return EP_OK;
+  if (!y || !ll_slot || !out) return EP_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out)) return EP_ERR_INVALID_ARG;
+  DeviceProps props;
+  if (!device_props(&props)) return EP_ERR_CUDA;
+  Args a = {};
+  a.y = static_cast<const uint16_t*>(y);
+  a.out = static_cast<uint16_t*>(out);
+  a.T = num_tokens;
+  a.H = hidden;
+  a.topk_w = topk_weights;
+  a.K = num_topk;
+  a.ll_slot = ll_slot;
+  a.err = err_word;
+  a.dmax = num_topk;
+  return launch_combine(a, props, stream);
 }

@@ -35,7 +35,9 @@ struct Args {
   const int64_t* topk_idx;
   const float* topk_w;
   int K, E, El, R;
-  const int32_t* slot;
+  const int32_t* dest;  // [T, ndest] destination rows, -1 = none
+  int ndest;            // R (rank-major layout) or K (expert-major layout)
+  bool rank_meta;       // write the per-row top-k metadata of the rank-major layout
   const int32_t* ntpe;
   int64_t cap;
   void* recv_x;
@@ -75,12 +77,12 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_kernel(Args a) {
   const int slice = (int)(gw % a.nslices);
   if (t >= a.T) return;  // uniform per warp
 
-  // destinations of this token, in rank order
+  // destinations of this token, in column order
   int nd = 0;
   bool over = false;
-  for (int r0 = 0; r0 < a.R; r0 += 32) {
+  for (int r0 = 0; r0 < a.ndest; r0 += 32) {
     const int r = r0 + lane;
-    const int32_t sl = r < a.R ? a.slot[t * a.R + r] : -1;
+    const int32_t sl = r < a.ndest ? a.dest[t * a.ndest + r] : -1;
     const bool ok = sl >= 0 && sl < a.cap;
     over |= sl >= a.cap;
     const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
@@ -97,7 +99,10 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_kernel(Args a) {
 
   // per-row metadata: source token, and the top-k entries that are local to
   // the destination (local expert id and weight), -1 / 0 elsewhere
-  if (slice == 0 && (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_w)) {
+  if (slice == 0 && !a.rank_meta && a.recv_src_idx) {
+    for (int d = lane; d < nd; d += 32) a.recv_src_idx[dst_row[warp][d]] = (int32_t)t;
+  }
+  if (slice == 0 && a.rank_meta && (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_w)) {
     const int64_t e = lane < a.K ? a.topk_idx[t * a.K + lane] : -1;
     const float w = (lane < a.K && a.topk_w) ? a.topk_w[t * a.K + lane] : 0.0f;
     const int er = (e >= 0 && e < a.E) ? (int)(e / a.El) : -1;
@@ -181,6 +186,34 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_kernel(Args a) {
 }
 
 }  // namespace
+
+// Slicing and launch shared by the rank-major and expert-major dispatch.
+// Small batches: several warps share a token (each a run of 32*kUnroll
+// vectors), aiming at four waves of 64 warps per SM.
+ep_status_t launch_dispatch(Args& a, bool fp8, ep_stream_t stream) {
+  DeviceProps props;
+  if (!device_props(&props)) return EP_ERR_CUDA;
+  const int64_t num_tokens = a.T;
+  const int nvec = a.H / 8;
+  const int max_slices = (nvec + 32 * kUnroll - 1) / (32 * kUnroll);
+  const int64_t want_warps = (int64_t)props.sm_count * 64 * 4;
+  int64_t ns = num_tokens > 0 ? (want_warps + num_tokens - 1) / num_tokens : 1;
+  a.nslices = (int)(ns < 1 ? 1 : (ns > max_slices ? max_slices : ns));
+  a.vps = ((nvec + a.nslices - 1) / a.nslices + 31) / 32 * 32;
+  a.nslices = (nvec + a.vps - 1) / a.vps;  // no empty slice
+  int64_t blocks = (num_tokens * a.nslices + kWarps - 1) / kWarps;
+  if (blocks == 0) {
+    if (!a.nrpe) return EP_OK;
+    blocks = 1;
+  }
+  cudaStream_t st = to_cuda(stream);
+  if (fp8)
+    dispatch_kernel<true><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
+  else
+    dispatch_kernel<false><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
+  return launch_status();
+}
+
 }  // namespace ep
 
 using namespace ep;
@@ -204,7 +237,7 @@ extern "C" ep_status_t ep_dispatch(const void* x, int hidden, const int64_t* top
     if (!aligned16(x) || !aligned16(recv_x)) return EP_ERR_INVALID_ARG;
   }
   if (num_recv_tokens_per_expert && !num_tokens_per_expert) return EP_ERR_INVALID_ARG;
-  Args a;
+  Args a = {};
   a.x = static_cast<const int4*>(x);
   a.T = num_tokens;
   a.H = hidden;
@@ -214,7 +247,9 @@ extern "C" ep_status_t ep_dispatch(const void* x, int hidden, const int64_t* top
   a.E = num_experts;
   a.El = num_experts / num_ranks;
   a.R = num_ranks;
-  a.slot = slot;
+  a.dest = slot;
+  a.ndest = num_ranks;
+  a.rank_meta = true;
   a.ntpe = num_tokens_per_expert;
   a.cap = recv_capacity_rows;
   a.recv_x = recv_x;
@@ -224,26 +259,33 @@ extern "C" ep_status_t ep_dispatch(const void* x, int hidden, const int64_t* top
   a.recv_topk_w = recv_topk_weights;
   a.nrpe = num_recv_tokens_per_expert;
   a.err = err_word;
-  // Small batches: several warps share a token (each a run of 32*kUnroll
-  // vectors), aiming at four waves of 64 warps per SM.
-  DeviceProps props;
-  if (!device_props(&props)) return EP_ERR_CUDA;
-  const int nvec = hidden / 8;
-  const int max_slices = (nvec + 32 * kUnroll - 1) / (32 * kUnroll);
-  const int64_t want_warps = (int64_t)props.sm_count * 64 * 4;
-  int64_t ns = num_tokens > 0 ? (want_warps + num_tokens - 1) / num_tokens : 1;
-  a.nslices = (int)(ns < 1 ? 1 : (ns > max_slices ? max_slices : ns));
-  a.vps = ((nvec + a.nslices - 1) / a.nslices + 31) / 32 * 32;
-  a.nslices = (nvec + a.vps - 1) / a.vps;  // no empty slice
-  int64_t blocks = (num_tokens * a.nslices + kWarps - 1) / kWarps;
-  if (blocks == 0) {
-    if (!a.nrpe) return EP_OK;
-    blocks = 1;
+  return launch_dispatch(a, use_fp8 != 0, stream);
+}
+
+extern "C" ep_status_t ep_ll_dispatch(const void* x, int hidden, int64_t num_tokens, int num_topk,
+                                      const int32_t* ll_slot, int64_t recv_capacity_rows,
+                                      int use_fp8, void* recv_x, float* recv_scales,
+                                      int32_t* recv_src_idx, int32_t* err_word,
+                                      ep_stream_t stream) {
+  if (num_tokens < 0 || num_topk < 1 || num_topk > EP_MAX_TOPK) return EP_ERR_INVALID_ARG;
+  if (hidden < 8 || hidden % 8 != 0 || (use_fp8 && hidden % 128 != 0)) return EP_ERR_INVALID_ARG;
+  if (recv_capacity_rows < 0 || recv_capacity_rows >= (int64_t(1) << 31)) return EP_ERR_INVALID_ARG;
+  if (num_tokens > 0) {
+    if (!x || !ll_slot || !recv_x || (use_fp8 && !recv_scales)) return EP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(recv_x)) return EP_ERR_INVALID_ARG;
   }
-  cudaStream_t st = to_cuda(stream);
-  if (use_fp8)
-    dispatch_kernel<true><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
-  else
-    dispatch_kernel<false><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
-  return launch_status();
+  Args a = {};
+  a.x = static_cast<const int4*>(x);
+  a.T = num_tokens;
+  a.H = hidden;
+  a.K = num_topk;
+  a.dest = ll_slot;
+  a.ndest = num_topk;
+  a.rank_meta = false;
+  a.cap = recv_capacity_rows;
+  a.recv_x = recv_x;
+  a.recv_scales = recv_scales;
+  a.recv_src_idx = recv_src_idx;
+  a.err = err_word;
+  return launch_dispatch(a, use_fp8 != 0, stream);
 }

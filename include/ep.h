@@ -213,6 +213,68 @@ ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk_idx,
                        int num_experts, int num_ranks, const int32_t* slot, void* out,
                        int32_t* err_word, ep_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Low-latency (expert-major) layout: the receive layout of the low-latency
+ * kernels ("[Not ready] MSCCLPP EP implementation", the low-latency port:
+ * dispatch<kUseFP8,...> and combine over per-expert buffers indexed
+ * [local_expert * num_ranks + dst_rank]).  Every unmasked top-k slot (t, k)
+ * has its own row in the buffer of expert e = topk_idx[t][k]; expert e owns
+ * rows [e*cap, (e+1)*cap) of one packed buffer of E*cap rows, packed by
+ * source rank, then token, then k.
+ * ------------------------------------------------------------------------ */
+
+/* Device scratch for ep_ll_get_dispatch_layout (0 for invalid sizes). */
+size_t ep_ll_workspace_bytes(int64_t num_tokens, int num_ranks, int num_experts);
+
+/*
+ * In (device): topk_idx [T, K] int64, -1 = masked.
+ * expert_capacity: rows per expert (cap); cap * E < 2^31.  T is the largest
+ *   count any expert can receive when each token names distinct experts.
+ * Out (device):
+ *   ll_slot [T, K] int32: row of slot (t, k), i.e.
+ *     e*cap + ll_src_offset[e][src(t)]
+ *     + #{(t', k') of src(t) before (t, k) in (token, k) order naming e};
+ *     -1 for masked slots, ids outside [-1, E) (EP_ERRBIT_BAD_EXPERT) and
+ *     positions >= cap (EP_ERRBIT_CAPACITY).
+ *   ll_count [E] int32: slots naming each expert, over all sources
+ *   ll_src_offset [E, R] int32 (nullable): first row of source s within
+ *     expert e's rows (relative to e*cap).
+ * workspace: ep_ll_workspace_bytes(T, R, E) bytes (EP_ERR_CAPACITY if less).
+ */
+ep_status_t ep_ll_get_dispatch_layout(const int64_t* topk_idx, int64_t num_tokens, int num_topk,
+                                      int num_experts, int num_ranks, int64_t expert_capacity,
+                                      int32_t* ll_slot, int32_t* ll_count, int32_t* ll_src_offset,
+                                      int32_t* err_word, void* workspace, size_t workspace_bytes,
+                                      ep_stream_t stream);
+
+/*
+ * Low-latency dispatch: for every slot with ll_slot[t][k] >= 0, row
+ * ll_slot[t][k] of recv_x receives token t, as a bf16 copy or (use_fp8) as
+ * E4M3 codes with recv_scales per 128 channels, with the same rounding as
+ * ep_dispatch; recv_src_idx[row] = t (nullable).  A token named by K experts
+ * is written K times.
+ * In (device): x [T, H] bf16, ll_slot [T, K].  Out (device): recv_x
+ * [capacity, H] (bf16 or bytes), recv_scales [capacity, H/128] f32 (FP8),
+ * recv_src_idx [capacity] int32.  Rows >= recv_capacity_rows are skipped
+ * and set EP_ERRBIT_CAPACITY.
+ */
+ep_status_t ep_ll_dispatch(const void* x, int hidden, int64_t num_tokens, int num_topk,
+                           const int32_t* ll_slot, int64_t recv_capacity_rows, int use_fp8,
+                           void* recv_x, float* recv_scales, int32_t* recv_src_idx,
+                           int32_t* err_word, ep_stream_t stream);
+
+/*
+ * Low-latency combine: out[t] = bf16_rne( sum over slots k with
+ * ll_slot[t][k] >= 0 of w[t][k] * float(y[ll_slot[t][k]]) ), accumulated in
+ * float32 (each expert's output row read once; with topk_weights == NULL
+ * every slot weighs 1).  In (device): y [rows, H] bf16 in the expert-major
+ * layout, topk_weights [T, K] f32 (nullable), ll_slot [T, K].  Out (device):
+ * out [T, H] bf16, every element written.  Staging as ep_combine.
+ */
+ep_status_t ep_ll_combine(const void* y, int hidden, const float* topk_weights,
+                          int64_t num_tokens, int num_topk, const int32_t* ll_slot, void* out,
+                          int32_t* err_word, ep_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

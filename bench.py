@@ -299,37 +299,82 @@ def run_ours(args, cfg: Config):
     idx = torch.from_numpy(case.topk_idx).to(dev)
     w = torch.from_numpy(case.topk_weights).to(dev)
     x = torch.from_numpy(case.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
-    cap = ep.worst_case_rows(T, K, R)
-    L = ep.alloc_layout(T, E, R, dev)
-    D = ep.alloc_dispatched(cap, H, K, E, R, cfg.fp8, dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    if cfg.fp8:
+    stream = torch.cuda.current_stream(dev)
+    from dataclasses import replace as _replace
+
+    if args.layout == "ht":
+        # rank-major: worst-case capacity T * min(K, R) rows, no host sync per step
+        cap = ep.worst_case_rows(T, K, R)
+        L = ep.alloc_layout(T, E, R, dev)
+        D = ep.alloc_dispatched(cap, H, K, E, R, cfg.fp8, dev)
+
+        def do_layout():
+            ep.get_dispatch_layout(idx, E, R, err=err, out=L)
+
+        def do_dispatch(a, b):
+            Lc = L if (a, b) == (0, T) else _replace(
+                L, slot=L.slot[a:b], is_token_in_rank=L.is_token_in_rank[a:b])
+            ep.dispatch(x[a:b], idx[a:b], w[a:b], Lc, use_fp8=cfg.fp8, err=err, out=D)
+
+        def do_combine(a, b):
+            Lc = L if (a, b) == (0, T) else _replace(
+                L, slot=L.slot[a:b], is_token_in_rank=L.is_token_in_rank[a:b])
+            ep.combine(Y, idx[a:b], w[a:b], Lc, err=err, out=out[a:b])
+
+        recv_rows = cap
+        recv_payload = D.recv_x
+    else:
+        # expert-major: T rows per expert (the worst case with distinct experts per
+        # token) when the buffers stay under 32 GB, else 1.25x the largest count
+        LL = ep.ll_get_dispatch_layout(idx, E, R, T)
+        torch.cuda.synchronize(dev)
+        max_count = int(LL.ll_count.max().item())
+        cap = T if E * T * H * 2 <= (32 << 30) else ((max_count * 5 // 4 + 63) // 64) * 64
+        LL = ep.alloc_ll_layout(T, K, E, R, cap, dev)
+        DL = None
+
+        def do_layout():
+            ep.ll_get_dispatch_layout(idx, E, R, err=err, out=LL)
+
+        def do_dispatch(a, b):
+            LLc = LL if (a, b) == (0, T) else _replace(LL, ll_slot=LL.ll_slot[a:b])
+            ep.ll_dispatch(x[a:b], LLc, use_fp8=cfg.fp8, err=err, out=DL)
+
+        def do_combine(a, b):
+            LLc = LL if (a, b) == (0, T) else _replace(LL, ll_slot=LL.ll_slot[a:b])
+            ep.ll_combine(Y, w[a:b], LLc, err=err, out=out[a:b])
+
+        do_layout()
+        DL = ep.ll_dispatch(x, LL, use_fp8=cfg.fp8, err=err)
+        recv_rows = E * cap
+        recv_payload = DL.recv_x
+
+    if cfg.fp8:  # combine is bf16 in: random expert outputs in the receive layout
         gen = torch.Generator(device=dev)
         gen.manual_seed(rcfg.seed)
-        Y = torch.randn((cap, H), generator=gen, device=dev).to(torch.bfloat16)
+        Y = torch.randn((recv_rows, H), generator=gen, device=dev).to(torch.bfloat16)
     else:
-        Y = D.recv_x
-
-    stream = torch.cuda.current_stream(dev)
+        Y = recv_payload
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        ep.get_dispatch_layout(idx, E, R, err=err, out=L)
+        do_layout()
         if ev is not None:
             ev[1].record(stream)
-        ep.dispatch(x, idx, w, L, use_fp8=cfg.fp8, err=err, out=D)
+        do_dispatch(0, T)
         if ev is not None:
             ev[2].record(stream)
-        ep.combine(Y, idx, w, L, err=err, out=out)
+        do_combine(0, T)
         if ev is not None:
             ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    P = ep.total_rows(L)
+    P = ep.total_rows(L) if args.layout == "ht" else int(LL.ll_count.sum().item())
     if int(err.item()) != 0:
         raise SystemExit(f"device error word {int(err.item())} after warm-up")
 
@@ -379,7 +424,6 @@ def run_ours(args, cfg: Config):
     ev_used = [torch.cuda.Event() for _ in range(n_chunks)]    # x chunk read by dispatch
     ev_done = [torch.cuda.Event() for _ in range(n_chunks)]    # out chunk computed
     ev_back = [torch.cuda.Event() for _ in range(n_chunks)]    # out chunk copied back
-    from dataclasses import replace as _replace
     first = [True]
 
     def e2e_step():
@@ -394,16 +438,15 @@ def run_ours(args, cfg: Config):
                     s_in.wait_event(ev_used[c])  # the previous step has read this x chunk
                 x[a:b].copy_(h_x[a:b], non_blocking=True)
                 ev_in[c].record(s_in)
-        ep.get_dispatch_layout(idx, E, R, err=err, out=L)
+        do_layout()
         for c in range(n_chunks):
             a, b = bounds[c], bounds[c + 1]
             stream.wait_event(ev_in[c])
-            Lc = _replace(L, slot=L.slot[a:b], is_token_in_rank=L.is_token_in_rank[a:b])
-            ep.dispatch(x[a:b], idx[a:b], w[a:b], Lc, use_fp8=cfg.fp8, err=err, out=D)
+            do_dispatch(a, b)
             ev_used[c].record(stream)
             if not first[0]:
                 stream.wait_event(ev_back[c])  # the previous step's copy of this out chunk is done
-            ep.combine(Y, idx[a:b], w[a:b], Lc, err=err, out=out[a:b])
+            do_combine(a, b)
             ev_done[c].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_done[c])
@@ -456,14 +499,14 @@ def run_ours(args, cfg: Config):
         kname = {"dispatch": "dispatch_kernel", "combine": "combine_kernel"}[dom]
         src = {"dispatch": "ep_dispatch.cu", "combine": "ep_combine.cu"}[dom]
         traffic = load_traffic(kname, cfg.name)
-        cpu = None if (args.no_cpu_baseline or world > 1) else cpu_baseline(case)
+        cpu = None if (args.no_cpu_baseline or world > 1 or args.layout == "ll") else cpu_baseline(case)
         line = {
             "metric": METRIC, "value": whole_job_tokens_per_s(T, world, ms), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3+bf16" if cfg.fp8 else "bf16",
             "data": "synthetic (seeded routing and N(0,1) hidden states; no dataset)",
-            "config": config_dict(cfg, P, cap, T * H * 2),
+            "config": dict(config_dict(cfg, P, recv_rows, T * H * 2), layout=args.layout),
             "hbm_gbs": gbs, "hbm_frac": gbs / peak, "peak_gbs": peak, "peak_kind": peak_kind,
             "roofline": {"bound": "hbm", "kernel": kname, "source": src,
                          "achieved": kern[dom]["gbs"], "peak": peak, "unit": "GB/s",
@@ -494,6 +537,8 @@ def main(argv=None):
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(CONFIGS))
     ap.add_argument("--tokens-per-rank", type=int, default=None,
                     help="scale the workload (same recipe) for profiling runs")
+    ap.add_argument("--layout", choices=["ht", "ll"], default="ht",
+                    help="receive layout: rank-major (ht, default) or expert-major (ll)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="token chunks the end-to-end step pipelines its copies over")

@@ -269,20 +269,31 @@ class LLLayout:
         return self.num_experts * self.expert_capacity
 
 
+def alloc_ll_layout(num_tokens: int, num_topk: int, num_experts: int, num_ranks: int,
+                    expert_capacity: int, device: torch.device) -> LLLayout:
+    ws = torch.empty(max(int(lib().ep_ll_workspace_bytes(num_tokens, num_ranks, num_experts)), 16),
+                     dtype=torch.uint8, device=device)
+    return LLLayout(torch.empty((num_tokens, num_topk), dtype=torch.int32, device=device),
+                    torch.empty(num_experts, dtype=torch.int32, device=device),
+                    torch.empty((num_experts, num_ranks), dtype=torch.int32, device=device),
+                    num_experts, num_ranks, int(expert_capacity), ws)
+
+
 def ll_get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int,
                            expert_capacity: int | None = None, *,
-                           err: torch.Tensor | None = None) -> LLLayout:
+                           err: torch.Tensor | None = None,
+                           out: LLLayout | None = None) -> LLLayout:
     """Rows of the expert-major layout (default capacity: T rows per expert)."""
     _need(topk_idx, "topk_idx", torch.int64)
     T, K = topk_idx.shape
-    cap = T if expert_capacity is None else int(expert_capacity)
+    if out is not None:
+        L = out
+        cap = L.expert_capacity
+    else:
+        cap = T if expert_capacity is None else int(expert_capacity)
+        L = alloc_ll_layout(T, K, num_experts, num_ranks, cap, topk_idx.device)
     dev = topk_idx.device
-    ws = torch.empty(max(int(lib().ep_ll_workspace_bytes(T, num_ranks, num_experts)), 16),
-                     dtype=torch.uint8, device=dev)
-    L = LLLayout(torch.empty((T, K), dtype=torch.int32, device=dev),
-                 torch.empty(num_experts, dtype=torch.int32, device=dev),
-                 torch.empty((num_experts, num_ranks), dtype=torch.int32, device=dev),
-                 num_experts, num_ranks, cap, ws)
+    ws = L.workspace
     if err is not None:
         _need(err, "err", torch.int32)
     _check(lib().ep_ll_get_dispatch_layout(

@@ -17,7 +17,7 @@
 //                and a per-expert counter in shared memory carries the rank
 //                across steps.  It writes each slot's rank within the chunk
 //                and the chunk's per-expert histogram.
-//   2. scan   -- one thread per expert: exclusive prefix over chunks, the
+//   2. scan   -- one warp per expert: exclusive prefix over chunks, the
 //                per-source offsets and the per-expert count.
 //   3. assign -- one thread per slot: e*cap + chunk offset + rank, with the
 //                capacity check.
@@ -86,26 +86,32 @@ __global__ void __launch_bounds__(32)
   for (int e = lane; e < g.E; e += 32) chunk_hist[(int64_t)ch * g.E + e] = cnt[e];
 }
 
+// One warp per expert: lanes own contiguous runs of chunks, a warp prefix
+// over the runs, then each lane writes its chunks' offsets.
 __global__ void __launch_bounds__(256)
     ll_scan_kernel(LLGeom g, const int32_t* __restrict__ chunk_hist, int32_t* __restrict__ chunk_off,
                    int32_t* __restrict__ ll_count, int32_t* __restrict__ ll_src_offset) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= g.E) return;
-  int run = 0;
-  for (int c0 = 0; c0 < g.nchunks; c0 += 8) {
-    int v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = c0 + u < g.nchunks ? chunk_hist[(int64_t)(c0 + u) * g.E + e] : 0;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int ch = c0 + u;
-      if (ch >= g.nchunks) break;
-      if (ch % g.ncps == 0 && ll_src_offset) ll_src_offset[(int64_t)e * g.R + ch / g.ncps] = run;
-      chunk_off[(int64_t)ch * g.E + e] = run;
-      run += v[u];
-    }
+  const int lane = threadIdx.x & 31;
+  const int e = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (e >= g.E) return;  // uniform per warp
+  const int seg = (g.nchunks + 31) / 32;
+  const int lo = min(g.nchunks, lane * seg), hi = min(g.nchunks, lo + seg);
+  int sum = 0;
+#pragma unroll 4
+  for (int ch = lo; ch < hi; ++ch) sum += chunk_hist[(int64_t)ch * g.E + e];
+  int incl = sum;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
   }
-  if (ll_count) ll_count[e] = run;
+  int run = incl - sum;
+  for (int ch = lo; ch < hi; ++ch) {
+    const int v = chunk_hist[(int64_t)ch * g.E + e];
+    if (ch % g.ncps == 0 && ll_src_offset) ll_src_offset[(int64_t)e * g.R + ch / g.ncps] = run;
+    chunk_off[(int64_t)ch * g.E + e] = run;
+    run += v;
+  }
+  if (lane == 31 && ll_count) ll_count[e] = incl;
 }
 
 __global__ void __launch_bounds__(256)
@@ -173,7 +179,7 @@ extern "C" ep_status_t ep_ll_get_dispatch_layout(const int64_t* topk_idx, int64_
   int32_t* hist = static_cast<int32_t*>(workspace);
   int32_t* off = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + half);
   ll_rank_kernel<<<g.nchunks, 32, sizeof(int32_t) * g.E, st>>>(topk_idx, g, ll_slot, hist, err_word);
-  ll_scan_kernel<<<(g.E + 255) / 256, 256, 0, st>>>(g, hist, off, ll_count, ll_src_offset);
+  ll_scan_kernel<<<(g.E * 32 + 255) / 256, 256, 0, st>>>(g, hist, off, ll_count, ll_src_offset);
   const int64_t n = g.T * g.K;
   ll_assign_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(topk_idx, g, off, ll_slot, err_word);
   return launch_status();

@@ -482,12 +482,17 @@ def run_ours(args, cfg: Config):
     if int(err.item()) != 0:
         raise SystemExit(f"device error word {int(err.item())}")
 
+    if args.layout == "ll":
+        layout_launches = 3  # rank, expert scan, assign
+    else:  # count + assign, with the scan folded in unless R * blocks > 8192 (T > 0)
+        nb = R * ((T // R + 511) // 512)
+        layout_launches = 2 if R * nb <= 8192 else 3
     if rank == 0:
         peak, peak_kind = load_peaks()
         ab = algorithmic_bytes(cfg, P)
         gbs = (ab["dispatch"] + ab["combine"]) / (ms / 1e3) / 1e9
         kern = {
-            "layout": {"ms": lay_ms, "bytes": ab["layout"], "launches_per_step": 3},
+            "layout": {"ms": lay_ms, "bytes": ab["layout"], "launches_per_step": layout_launches},
             "dispatch": {"ms": dis_ms, "bytes": ab["dispatch"], "launches_per_step": 1,
                          "gbs": ab["dispatch"] / (dis_ms / 1e3) / 1e9},
             "combine": {"ms": com_ms, "bytes": ab["combine"], "launches_per_step": 1,
@@ -518,7 +523,7 @@ def run_ours(args, cfg: Config):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "steps": e2e_steps, "token_chunks": n_chunks,
                     "check": e2e_check},
-            "gpu_launches": 5 * args.steps,
+            "gpu_launches": (layout_launches + 2) * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

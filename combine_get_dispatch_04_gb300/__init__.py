@@ -35,7 +35,7 @@ EP_MAX_EXPERTS = 4096
 EXPORTED = ("ep_status_string", "ep_workspace_bytes", "ep_get_dispatch_layout",
             "ep_get_dispatch_layout_noalloc", "ep_layout_total_rows", "ep_dispatch",
             "ep_combine", "ep_ll_workspace_bytes", "ep_ll_get_dispatch_layout",
-            "ep_ll_dispatch", "ep_ll_combine")
+            "ep_ll_dispatch", "ep_ll_combine", "ep_debug_set_combine_stall")
 
 _lib = None
 
@@ -64,6 +64,8 @@ def load(path: str | None = None) -> C.CDLL:
     L.ep_dispatch.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, i64, i32, P, P, P, P, P,
                               P, P, P]
     L.ep_combine.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, P, P]
+    L.ep_debug_set_combine_stall.argtypes = [i32]
+    L.ep_debug_set_combine_stall.restype = None
     L.ep_ll_workspace_bytes.argtypes = [i64, i32, i32]
     L.ep_ll_workspace_bytes.restype = sz
     L.ep_ll_get_dispatch_layout.argtypes = [P, i64, i32, i32, i32, i64, P, P, P, P, P, sz, P]

@@ -68,6 +68,7 @@ struct Args {
   int S;       // pipeline stages
   int dmax;    // rows per stage = min(K, R)
   uint32_t stage_bytes;
+  int stall_unit;  // test hook: CTA 0 never arms this pipeline unit (-1: off)
 };
 
 // Offsets of the shared-memory regions that follow the S row tiles.
@@ -293,6 +294,10 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
           }
           const int c0 = c * a.C;
           const int clen = min(a.C, a.H - c0);
+          if (blockIdx.x == 0 && (int)it == a.stall_unit) {  // test hook: leave it unarmed
+            ++it;
+            continue;
+          }
           if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(D * clen * 2));
           __syncwarp();
           if (lane < D)
@@ -399,7 +404,11 @@ bool make_plan(int H, int K, int R, const DeviceProps& p, Plan* out) {
 
 // Plan, occupancy-sized persistent grid and launch, shared by the rank-major
 // and expert-major combine.
+thread_local int g_stall_unit = -1;  // set by ep_debug_set_combine_stall, used once
+
 ep_status_t launch_combine(Args& a, const DeviceProps& props, ep_stream_t stream) {
+  a.stall_unit = g_stall_unit;
+  g_stall_unit = -1;
   Plan plan;
   if (!make_plan(a.H, a.dmax, a.dmax, props, &plan)) return EP_ERR_INVALID_ARG;
   a.C = plan.C;
@@ -478,3 +487,5 @@ extern "C" ep_status_t ep_ll_combine(const void* y, int hidden, const float* top
   a.dmax = num_topk;
   return launch_combine(a, props, stream);
 }
+
+extern "C" void ep_debug_set_combine_stall(int unit) { ep::g_stall_unit = unit; }

@@ -275,6 +275,17 @@ ep_status_t ep_ll_combine(const void* y, int hidden, const float* topk_weights,
                           int64_t num_tokens, int num_topk, const int32_t* ll_slot, void* out,
                           int32_t* err_word, ep_stream_t stream);
 
+/*
+ * Test hook for the bounded waits of the combine pipeline (ep_combine and
+ * ep_ll_combine).  The next combine launched from this host thread leaves
+ * pipeline unit `unit` of CTA 0 unarmed, so the waits on it run out after
+ * about 1 s.  The launch then reports EP_ERRBIT_TIMEOUT in the error word,
+ * its output is incomplete, and it returns.  The hook is one-shot; -1
+ * cancels it.  It faults, traps and hangs nothing, and exists only so that
+ * tests can exercise the timeout path.
+ */
+void ep_debug_set_combine_stall(int unit);
+
 #ifdef __cplusplus
 }
 #endif

@@ -206,3 +206,37 @@ def test_combine_unweighted_full_skewed(ep):
             p = sub[a:b, r]
             bound[p >= 0] += yv[p[p >= 0]]
         assert_combine_close(bits_of(out[a:b]), want, bound)
+
+
+def test_combine_bounded_wait_reports_timeout_and_recovers(ep):
+    """A pipeline unit that is never armed (test hook) makes the combine's
+    bounded waits run out: the launch ends by itself with EP_ERRBIT_TIMEOUT in
+    the error word, and the next combine on the same context is correct."""
+    import time
+    cfg = CONFIGS["tiny"]
+    c = make_case(cfg)
+    idx, w, x = device_inputs(c)
+    L = ep.get_dispatch_layout(idx, cfg.num_experts, cfg.num_ranks)
+    d = ep.dispatch(x, idx, w, L)
+    torch.cuda.synchronize()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.lib().ep_debug_set_combine_stall(0)
+    t0 = time.time()
+    ep.combine(d.recv_x, idx, w, L, err=err)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    assert int(err.item()) & ep.EP_ERRBIT_TIMEOUT
+    assert elapsed < 10, elapsed
+    # the context is intact: a normal combine matches the oracle
+    err.zero_()
+    out = ep.combine(d.recv_x, idx, w, L, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    slot = L.slot.cpu().numpy()
+    P = ep.total_rows(L)
+    want = oracle.combine(bits_of(d.recv_x[:P]), c.topk_idx, c.topk_weights, cfg.num_experts,
+                          cfg.num_ranks, slot)
+    bound = combine_bound(oracle.bf16_to_double(bits_of(d.recv_x[:P])), c.topk_idx,
+                          c.topk_weights, slot, cfg.num_experts // cfg.num_ranks,
+                          np.arange(cfg.num_tokens))
+    assert_combine_close(bits_of(out), want, bound)

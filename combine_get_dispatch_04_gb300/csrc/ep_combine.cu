@@ -170,51 +170,77 @@ __device__ __forceinline__ int gather_token(const Args& a, int64_t t, int32_t* r
   return D;
 }
 
-// out[ch..ch+8) of one staged (token, chunk): sum over the token's D staged
-// rows of W[d] * row_d, in float32.  With kDMax > 0 (D <= kDMax) the D shared
-// loads are issued back to back from unrolled code; kDMax == 0 is the
-// general loop.
-template <int kDMax>
-__device__ __forceinline__ int4 reduce_rows(const uint8_t* stage, int C, int ch, int D,
-                                            const float* Wreg, const float* Wsm) {
-  float acc[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+// kP passes of one staged (token, chunk): for ch = ch0 + p*step (p < kP,
+// ch < clen), out[ch..ch+8) = sum over the token's D staged rows of
+// W[d] * row_d, in float32, stored as bf16.  With kDMax > 0 (D <= kDMax) the
+// shared loads of all kP passes are issued together from unrolled code;
+// kDMax == 0 is the general loop.
+template <int kDMax, int kP>
+__device__ __forceinline__ void reduce_rows(const uint8_t* stage, int C, int ch0, int step,
+                                            int clen, int D, const float* Wreg, const float* Wsm,
+                                            uint16_t* orow) {
   if constexpr (kDMax > 0) {
-    int4 v[kDMax];
+    int4 v[kP][kDMax];
 #pragma unroll
-    for (int d = 0; d < kDMax; ++d)
-      if (d < D) v[d] = *reinterpret_cast<const int4*>(stage + ((size_t)d * C + ch) * 2);
+    for (int p = 0; p < kP; ++p) {
+      const int ch = ch0 + p * step;
 #pragma unroll
-    for (int d = 0; d < kDMax; ++d) {
-      if (d < D) {
-        float f[8];
-        unpack_bf16x8(v[d], f);
+      for (int d = 0; d < kDMax; ++d)
+        if (ch < clen && d < D) v[p][d] = *reinterpret_cast<const int4*>(stage + ((size_t)d * C + ch) * 2);
+    }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = fmaf(Wreg[d], f[q], acc[q]);
+    for (int p = 0; p < kP; ++p) {
+      const int ch = ch0 + p * step;
+      if (ch >= clen) break;
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+      for (int d = 0; d < kDMax; ++d) {
+        if (d < D) {
+          float f[8];
+          unpack_bf16x8(v[p][d], f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = fmaf(Wreg[d], f[q], acc[q]);
+        }
       }
+      int4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+        ow[q] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      st_stream_v4(reinterpret_cast<int4*>(orow + ch), o);
     }
   } else {
-    for (int d = 0; d < D; ++d) {
-      const int4 v = *reinterpret_cast<const int4*>(stage + ((size_t)d * C + ch) * 2);
-      const float wd = Wsm[d];
-      float f[8];
-      unpack_bf16x8(v, f);
+    for (int p = 0; p < kP; ++p) {
+      const int ch = ch0 + p * step;
+      if (ch >= clen) break;
+      float acc[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = fmaf(wd, f[q], acc[q]);
+      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+      for (int d = 0; d < D; ++d) {
+        const int4 v = *reinterpret_cast<const int4*>(stage + ((size_t)d * C + ch) * 2);
+        const float wd = Wsm[d];
+        float f[8];
+        unpack_bf16x8(v, f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = fmaf(wd, f[q], acc[q]);
+      }
+      int4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+        ow[q] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      st_stream_v4(reinterpret_cast<int4*>(orow + ch), o);
     }
   }
-  int4 o;
-  uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const __nv_bfloat162 p = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-    ow[q] = *reinterpret_cast<const uint32_t*>(&p);
-  }
-  return o;
 }
 
-template <int kDMax>
+template <int kDMax, int kP>
 __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const SmemLayout lay = smem_layout(a.S, a.stage_bytes, a.dmax);
@@ -345,9 +371,9 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
           const int c0 = c * a.C;
           const int clen = min(a.C, a.H - c0);
           const uint8_t* stage = tiles + (size_t)s * a.stage_bytes;
-          for (int ch = ct * 8; ch < clen; ch += kConsumerWarps * 32 * 8)
-            *reinterpret_cast<int4*>(orow + c0 + ch) =
-                reduce_rows<kDMax>(stage, a.C, ch, D, Wreg, Wsm);
+          constexpr int kStep = kConsumerWarps * 32 * 8;
+          for (int ch = ct * 8; ch < clen; ch += kP * kStep)
+            reduce_rows<kDMax, kP>(stage, a.C, ch, kStep, clen, D, Wreg, Wsm, orow + c0);
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);
           ++it;
@@ -415,8 +441,12 @@ ep_status_t launch_combine(Args& a, const DeviceProps& props, ep_stream_t stream
   a.S = plan.S;
   a.stage_bytes = plan.stage_bytes;
   a.nchunk = (a.H + a.C - 1) / a.C;
-  // rows per token <= 8 (every workload here): unrolled reduction
-  void (*kernel)(Args) = a.dmax <= 8 ? combine_kernel<8> : combine_kernel<0>;
+  // unrolled reductions for up to 8 rows per token (every workload here),
+  // with more passes in flight when there are fewer rows
+  void (*kernel)(Args) = a.dmax <= 2   ? combine_kernel<2, 4>
+                         : a.dmax <= 4 ? combine_kernel<4, 2>
+                         : a.dmax <= 8 ? combine_kernel<8, 1>
+                                       : combine_kernel<0, 1>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)plan.smem) != cudaSuccess)
     return EP_ERR_CUDA;

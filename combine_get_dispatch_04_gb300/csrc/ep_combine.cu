@@ -242,6 +242,7 @@ __device__ __forceinline__ void reduce_rows(const uint8_t* stage, int C, int ch0
 
 template <int kDMax, int kP>
 __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
+  pdl_wait_then_release();
   extern __shared__ __align__(128) uint8_t smem[];
   const SmemLayout lay = smem_layout(a.S, a.stage_bytes, a.dmax);
   uint8_t* tiles = smem;
@@ -458,7 +459,7 @@ ep_status_t launch_combine(Args& a, const DeviceProps& props, ep_stream_t stream
   const int64_t ctas =
       (int64_t)props.sm_count * (resident < plan.ctas_per_sm ? resident : plan.ctas_per_sm);
   const int64_t grid = a.T < ctas ? a.T : ctas;
-  kernel<<<(unsigned)grid, kThreads, plan.smem, to_cuda(stream)>>>(a);
+  launch_pdl(kernel, (unsigned)grid, kThreads, plan.smem, to_cuda(stream), a);
   return launch_status();
 }
 

@@ -42,9 +42,38 @@ inline bool routing_ok(int64_t T, int K, int E, int R) {
   return true;
 }
 
+// Launch with programmatic dependent launch (PDL): the kernel may be
+// scheduled while the previous kernel in the stream finishes, and waits for
+// it in pdl_wait() before touching global memory.  Every kernel of this
+// library calls pdl_wait() before its first global access, so all data
+// dependences between consecutive launches are kept.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------------------
 // device side
 // ---------------------------------------------------------------------------
+
+// Waits until the previous kernel in the stream has completed and its
+// memory is visible (a no-op without PDL), then lets the next kernel be
+// scheduled as this grid's blocks retire.
+__device__ __forceinline__ void pdl_wait_then_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // bounded pipeline waits: 1 s
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

@@ -59,6 +59,7 @@ __device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float 
 
 template <bool kFP8>
 __global__ void __launch_bounds__(kWarps * 32) dispatch_kernel(Args a) {
+  pdl_wait_then_release();
   __shared__ int32_t dst_row[kWarps][EP_MAX_RANKS];
   __shared__ int32_t dst_rank[kWarps][EP_MAX_RANKS];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -208,9 +209,9 @@ ep_status_t launch_dispatch(Args& a, bool fp8, ep_stream_t stream) {
   }
   cudaStream_t st = to_cuda(stream);
   if (fp8)
-    dispatch_kernel<true><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
+    launch_pdl(dispatch_kernel<true>, (unsigned)blocks, kWarps * 32, 0, st, a);
   else
-    dispatch_kernel<false><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
+    launch_pdl(dispatch_kernel<false>, (unsigned)blocks, kWarps * 32, 0, st, a);
   return launch_status();
 }
 

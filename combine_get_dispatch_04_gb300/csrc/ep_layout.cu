@@ -90,6 +90,7 @@ __device__ __forceinline__ void write_member_row(uint8_t* row, uint64_t mask, in
 __global__ void __launch_bounds__(kTok)
     layout_count_kernel(const int64_t* __restrict__ topk_idx, Geom g,
                         uint8_t* __restrict__ is_token_in_rank, Workspace ws, int32_t* err) {
+  pdl_wait_then_release();
   extern __shared__ int32_t smem[];
   int32_t* hist = smem;                // [E]
   int32_t* warp_cnt = smem + g.E;      // [kTokWarps][R]
@@ -165,6 +166,7 @@ __device__ __forceinline__ int strided_sum(const int32_t* p, int n, int64_t stri
 __global__ void __launch_bounds__(kScanThreads)
     layout_scan_kernel(Geom g, Workspace ws, int32_t* __restrict__ ntpr,
                        int32_t* __restrict__ ntpe, int32_t* __restrict__ recv_base) {
+  pdl_wait_then_release();
   __shared__ int32_t recv_count[EP_MAX_RANKS];
   __shared__ int32_t base[EP_MAX_RANKS + 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -230,6 +232,7 @@ __global__ void __launch_bounds__(kTok)
     layout_assign_kernel(Geom g, Workspace ws, int32_t* __restrict__ slot, bool fold,
                          int32_t* __restrict__ ntpr, int32_t* __restrict__ ntpe,
                          int32_t* __restrict__ recv_base) {
+  pdl_wait_then_release();
   __shared__ int32_t warp_off[kTokWarps][EP_MAX_RANKS];
   __shared__ int32_t blk_pre[EP_MAX_RANKS];
   __shared__ int32_t tot[EP_MAX_RANKS];
@@ -329,12 +332,12 @@ void launch_layout(const int64_t* topk_idx, const Geom& g, const Workspace& ws,
                    int32_t* recv_base, int32_t* err_word, cudaStream_t st) {
   if (g.nb > 0) {
     const size_t smem = sizeof(int32_t) * ((size_t)g.E + (size_t)kTokWarps * g.R);
-    layout_count_kernel<<<g.nb, kTok, smem, st>>>(topk_idx, g, is_token_in_rank, ws, err_word);
+    launch_pdl(layout_count_kernel, g.nb, kTok, smem, st, topk_idx, g, is_token_in_rank, ws, err_word);
   }
   const bool fold = g.nb > 0 && (int64_t)g.R * g.nb <= kFoldMax;
-  if (!fold) layout_scan_kernel<<<1, kScanThreads, 0, st>>>(g, ws, ntpr, ntpe, recv_base);
+  if (!fold) launch_pdl(layout_scan_kernel, 1, kScanThreads, 0, st, g, ws, ntpr, ntpe, recv_base);
   if (g.nb > 0)
-    layout_assign_kernel<<<g.nb, kTok, 0, st>>>(g, ws, slot, fold, ntpr, ntpe, recv_base);
+    launch_pdl(layout_assign_kernel, g.nb, kTok, 0, st, g, ws, slot, fold, ntpr, ntpe, recv_base);
 }
 
 }  // namespace

@@ -54,6 +54,7 @@ size_t ll_ws_bytes(const LLGeom& g) { return 2 * align_up(sizeof(int32_t) * (siz
 __global__ void __launch_bounds__(32)
     ll_rank_kernel(const int64_t* __restrict__ topk_idx, LLGeom g, int32_t* __restrict__ ll_slot,
                    int32_t* __restrict__ chunk_hist, int32_t* err) {
+  pdl_wait_then_release();
   extern __shared__ int32_t cnt[];  // [E]
   const int lane = threadIdx.x;
   const int ch = blockIdx.x;
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(32)
 __global__ void __launch_bounds__(256)
     ll_scan_kernel(LLGeom g, const int32_t* __restrict__ chunk_hist, int32_t* __restrict__ chunk_off,
                    int32_t* __restrict__ ll_count, int32_t* __restrict__ ll_src_offset) {
+  pdl_wait_then_release();
   const int lane = threadIdx.x & 31;
   const int e = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (e >= g.E) return;  // uniform per warp
@@ -118,6 +120,7 @@ __global__ void __launch_bounds__(256)
     ll_assign_kernel(const int64_t* __restrict__ topk_idx, LLGeom g,
                      const int32_t* __restrict__ chunk_off, int32_t* __restrict__ ll_slot,
                      int32_t* err) {
+  pdl_wait_then_release();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   bool over = false;
   if (i < g.T * g.K) {
@@ -178,9 +181,12 @@ extern "C" ep_status_t ep_ll_get_dispatch_layout(const int64_t* topk_idx, int64_
   }
   int32_t* hist = static_cast<int32_t*>(workspace);
   int32_t* off = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + half);
-  ll_rank_kernel<<<g.nchunks, 32, sizeof(int32_t) * g.E, st>>>(topk_idx, g, ll_slot, hist, err_word);
-  ll_scan_kernel<<<(g.E * 32 + 255) / 256, 256, 0, st>>>(g, hist, off, ll_count, ll_src_offset);
+  launch_pdl(ll_rank_kernel, g.nchunks, 32, sizeof(int32_t) * g.E, st, topk_idx, g, ll_slot, hist,
+             err_word);
+  launch_pdl(ll_scan_kernel, (g.E * 32 + 255) / 256, 256, 0, st, g, hist, off, ll_count,
+             ll_src_offset);
   const int64_t n = g.T * g.K;
-  ll_assign_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(topk_idx, g, off, ll_slot, err_word);
+  launch_pdl(ll_assign_kernel, (unsigned)((n + 255) / 256), 256, 0, st, topk_idx, g, off, ll_slot,
+             err_word);
   return launch_status();
 }

@@ -251,6 +251,8 @@ def run_reference(args, cfg: Config):
     if rank != 0:
         return
     case = make_case(cfg)
+    import oracle
+    P = oracle.layout(case.topk_idx, cfg.num_experts, cfg.num_ranks).num_rows
     budget = 150.0
     per_step = budget / max(1, args.steps + args.warmup)
     n = calibrate_sample(case, per_step)
@@ -265,7 +267,8 @@ def run_reference(args, cfg: Config):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; no dataset)",
-        "config": config_dict(cfg, -1, -1, cfg.num_tokens * cfg.hidden * 2),
+        "config": dict(config_dict(cfg, P, cfg.num_tokens * min(cfg.num_topk, cfg.num_ranks),
+                                   cfg.num_tokens * cfg.hidden * 2), layout="ht"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"each step: first {n} tokens of each source rank "
                                    f"({sub.cfg.num_tokens} tokens), single-threaded C oracle"},

@@ -104,3 +104,19 @@ def test_layout_on_a_side_stream(ep):
         L = ep.get_dispatch_layout(idx, cfg.num_experts, cfg.num_ranks)
     s.synchronize()
     compare_layout(L, oracle.layout(c.topk_idx, cfg.num_experts, cfg.num_ranks))
+
+
+def test_layout_unfolded_scan_path(ep):
+    """64 ranks x 2048 tokens per rank give 64 * 256 blocks > 8192, so the
+    layout runs the separate scan kernel between count and assign."""
+    from workloads import Config
+    cfg = Config("r64_unfolded", 64, 2048, 8, 128, 4, routing="zipf", zipf_s=1.2,
+                 mask_prob=0.05, seed=901)
+    c = make_case(cfg, with_hidden=False)
+    idx, _, _ = device_inputs(c)
+    L = ep.alloc_layout(cfg.num_tokens, cfg.num_experts, cfg.num_ranks, idx.device)
+    poison_layout(L)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.get_dispatch_layout(idx, cfg.num_experts, cfg.num_ranks, err=err, out=L)
+    compare_layout(L, oracle.layout(c.topk_idx, cfg.num_experts, cfg.num_ranks))
+    assert int(err.item()) == 0

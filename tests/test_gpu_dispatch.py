@@ -183,3 +183,38 @@ def test_dispatch_bf16_full_size(ep, name):
         np.testing.assert_array_equal(out.recv_topk_weights[o].cpu().numpy().view(np.uint32),
                                       want.recv_topk_weights[compact].view(np.uint32))
     assert P <= out.recv_x.shape[0]
+
+
+def test_dispatch_fp8_every_bf16_value(ep):
+    """Every finite bf16 value with |x| <= 448 quantised by the device: each
+    128-channel block holds +448 (so amax = 448 and the multiplier 448/a is
+    exactly 1) and 127 of the values.  The device's E4M3 codes must equal the
+    oracle's for all of them, ties at E4M3 midpoints, zeros and subnormals
+    included."""
+    from workloads import Config
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.bf16_to_double(codes)
+    keep = np.isfinite(vals) & (np.abs(vals) <= 448.0)
+    pats = codes[keep]
+    per_block = 127
+    nblk = -(-pats.size // per_block)
+    blocks = np.zeros((nblk, 128), np.uint16)
+    blocks[:, 0] = 0x43E0  # +448.0
+    flat = np.full(nblk * per_block, 0x3F80, np.uint16)  # pad with 1.0
+    flat[:pats.size] = pats
+    blocks[:, 1:] = flat.reshape(nblk, per_block)
+    H = 1024
+    T = -(-nblk * 128 // H)
+    x_bits = np.full(T * H, 0x3F80, np.uint16)
+    x_bits[:blocks.size] = blocks.ravel()
+    x_bits = x_bits.reshape(T, H)
+    # route every token to expert 0 of a single rank
+    cfg = Config("fp8_all_bf16", 1, T, H, 1, 1, fp8=True, seed=0)
+    c = make_case(cfg)
+    c.x_bits = x_bits
+    c.topk_idx[:] = 0
+    L, P, got, err = run_dispatch(ep, cfg, c, use_fp8=True)
+    assert err == 0 and P == T
+    check_against_oracle(cfg, c, L, P, got, use_fp8=True)
+    # and the blocks with amax 448 have scale exactly 1
+    assert bool((got.recv_scales[:P].reshape(-1)[:nblk] == 1.0).all())

@@ -12,8 +12,11 @@
 // vectors of the row (8 bf16 channels); kUnroll vectors per lane are loaded
 // before the stores so each warp keeps 4 x 512 bytes of reads in flight.  Loads bypass L1, stores use
 // the streaming policy.  In the FP8 variant a half-warp holds one block of
-// 128 channels: its amax is a 4-step xor-shuffle reduction, and the block is
-// quantised in registers before being written to every destination.  The
+// 128 channels: its amax is taken on the raw bf16 bits (per-halfword unsigned
+// max of |x|, then a 4-step xor-shuffle), one lane per block computes the
+// block's two divisions (a warp's 8 blocks in one instruction sequence), and
+// the block is quantised in registers before being written to every
+// destination.  The
 // quantiser rounds exactly as the format definition requires: 448/a and a/448
 // are single correctly rounded divisions (__fdiv_rn), x * (448/a) is a single
 // multiply (__fmul_rn), and the E4M3 conversion is the hardware's
@@ -148,22 +151,43 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_kernel(Args a) {
     uint8_t* out = reinterpret_cast<uint8_t*>(a.recv_x);
     const int nblk = a.H / 128;
     for (int v0 = vbeg; v0 < vend; v0 += 32 * kUnroll) {
+      int4 raw[kUnroll];
+      uint32_t mbits[kUnroll];  // amax of the lane's block, as bf16 bits
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v = v0 + u * 32 + lane;
+        raw[u] = v < vend ? ld_stream_v4(src + v) : make_int4(0, 0, 0, 0);
+        // for finite bf16 the order of |x| is the unsigned order of the low
+        // 15 bits, so a per-halfword unsigned max gives the exact amax bits
+        uint32_t m = __vmaxu2(__vmaxu2((uint32_t)raw[u].x & 0x7FFF7FFFu, (uint32_t)raw[u].y & 0x7FFF7FFFu),
+                              __vmaxu2((uint32_t)raw[u].z & 0x7FFF7FFFu, (uint32_t)raw[u].w & 0x7FFF7FFFu));
+        m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        mbits[u] = m;
+      }
+      // one correctly rounded division pair for the warp's 2*kUnroll blocks:
+      // lane 2u+h takes block (u, half-warp h), then hands the results back
+      uint32_t mine = 0;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t lo = __shfl_sync(0xFFFFFFFFu, mbits[u], 0);
+        const uint32_t hi = __shfl_sync(0xFFFFFFFFu, mbits[u], 16);
+        if (lane == 2 * u) mine = lo;
+        if (lane == 2 * u + 1) mine = hi;
+      }
+      const float am = fmaxf(__uint_as_float(mine << 16), 1e-4f);
+      const float sc = __fdiv_rn(am, 448.0f);
+      const float iv = __fdiv_rn(448.0f, am);
       uint2 q[kUnroll];
       float scale[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
-        const int v = v0 + u * 32 + lane;
+        const int owner = 2 * u + (lane >> 4);
+        const float inv = __shfl_sync(0xFFFFFFFFu, iv, owner);
+        scale[u] = __shfl_sync(0xFFFFFFFFu, sc, owner);
         float f[8];
-        const int4 raw = v < vend ? ld_stream_v4(src + v) : make_int4(0, 0, 0, 0);
-        unpack_bf16x8(raw, f);
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        const float am = fmaxf(amax, 1e-4f);
-        scale[u] = __fdiv_rn(am, 448.0f);
-        const float inv = __fdiv_rn(448.0f, am);
+        unpack_bf16x8(raw[u], f);
         q[u].x = cvt_e4m3x4(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
                             __fmul_rn(f[3], inv));
         q[u].y = cvt_e4m3x4(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv), __fmul_rn(f[6], inv),

@@ -68,20 +68,31 @@ __global__ void __launch_bounds__(32)
   bool bad = false;
   const int64_t* base = topk_idx + t0 * g.K;  // the chunk's slots are contiguous
   int32_t* out = ll_slot + t0 * g.K;
-  for (int64_t j0 = 0; j0 < nslots; j0 += 32) {
-    const int64_t j = j0 + lane;
-    const int64_t e = j < nslots ? base[j] : -1;
-    int key = -1;
-    if (e >= 0 && e < g.E)
-      key = (int)e;
-    else if (j < nslots && e != -1)
-      bad = true;
-    const unsigned peers = __match_any_sync(0xFFFFFFFFu, key);
-    const int before = key >= 0 ? cnt[key] : 0;
-    __syncwarp();
-    if (key >= 0 && lane == __ffs(peers) - 1) cnt[key] = before + __popc(peers);
-    __syncwarp();
-    if (j < nslots) out[j] = key >= 0 ? before + __popc(peers & lt) : -1;
+  for (int64_t j00 = 0; j00 < nslots; j00 += 32 * 8) {
+    int64_t ev[8];  // eight steps of ids loaded before any is used
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t j = j00 + u * 32 + lane;
+      ev[u] = j < nslots ? base[j] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t j0 = j00 + u * 32;
+      if (j0 >= nslots) break;  // uniform
+      const int64_t j = j0 + lane;
+      const int64_t e = ev[u];
+      int key = -1;
+      if (e >= 0 && e < g.E)
+        key = (int)e;
+      else if (j < nslots && e != -1)
+        bad = true;
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, key);
+      const int before = key >= 0 ? cnt[key] : 0;
+      __syncwarp();
+      if (key >= 0 && lane == __ffs(peers) - 1) cnt[key] = before + __popc(peers);
+      __syncwarp();
+      if (j < nslots) out[j] = key >= 0 ? before + __popc(peers & lt) : -1;
+    }
   }
   if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && err) atomicOr(err, EP_ERRBIT_BAD_EXPERT);
   for (int e = lane; e < g.E; e += 32) chunk_hist[(int64_t)ch * g.E + e] = cnt[e];

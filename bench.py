@@ -317,7 +317,7 @@ def run_ours(args, cfg: Config):
         D = ep.alloc_dispatched(cap, H, K, E, R, cfg.fp8, dev)
 
         def do_layout():
-            ep.get_dispatch_layout(idx, E, R, err=err, out=L)
+            ep.get_dispatch_layout(idx, E, R, err=err, out=L, path=args.layout_kernels)
 
         def do_dispatch(a, b):
             Lc = L if (a, b) == (0, T) else _replace(
@@ -500,11 +500,15 @@ def run_ours(args, cfg: Config):
     if int(err.item()) != 0:
         raise SystemExit(f"device error word {int(err.item())}")
 
+    layout_kernels = None
     if args.layout == "ll":
         layout_launches = 3  # rank, expert scan, assign
+    elif args.layout_kernels == "single" or (args.layout_kernels == "auto"
+                                             and ep.auto_single_launch(T, R, E)):
+        layout_launches, layout_kernels = 1, "single"  # one thread-block cluster
     else:  # count + assign, with the scan folded in unless R * blocks > 8192 (T > 0)
         nb = R * ((T // R + 511) // 512)
-        layout_launches = 2 if R * nb <= 8192 else 3
+        layout_launches, layout_kernels = (2 if R * nb <= 8192 else 3), "multi"
     if rank == 0:
         peak, peak_kind = load_peaks()
         ab = algorithmic_bytes(cfg, P)
@@ -529,7 +533,8 @@ def run_ours(args, cfg: Config):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3+bf16" if cfg.fp8 else "bf16",
             "data": "synthetic (seeded routing and N(0,1) hidden states; no dataset)",
-            "config": dict(config_dict(cfg, P, recv_rows, T * H * 2), layout=args.layout),
+            "config": dict(config_dict(cfg, P, recv_rows, T * H * 2), layout=args.layout,
+                           **({"layout_kernels": layout_kernels} if layout_kernels else {})),
             "hbm_gbs": gbs, "hbm_frac": gbs / peak, "peak_gbs": peak, "peak_kind": peak_kind,
             "roofline": {"bound": "hbm", "kernel": kname, "source": src,
                          "achieved": kern[dom]["gbs"], "peak": peak, "unit": "GB/s",
@@ -562,6 +567,9 @@ def main(argv=None):
                     help="scale the workload (same recipe) for profiling runs")
     ap.add_argument("--layout", choices=["ht", "ll"], default="ht",
                     help="receive layout: rank-major (ht, default) or expert-major (ll)")
+    ap.add_argument("--layout-kernels", choices=["auto", "multi", "single"], default="auto",
+                    help="rank-major layout kernels: one cluster launch (single, small "
+                         "batches), the multi-launch form, or the library's choice (auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="token chunks the end-to-end step pipelines its copies over")

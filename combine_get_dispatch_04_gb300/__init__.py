@@ -31,8 +31,13 @@ EP_MAX_RANKS = 64
 EP_MAX_TOPK = 32
 EP_MAX_EXPERTS = 4096
 
+# ep_layout_path_t
+LAYOUT_PATHS = {"auto": 0, "multi": 1, "single": 2}
+
 # every entry point declared in include/ep.h
 EXPORTED = ("ep_status_string", "ep_workspace_bytes", "ep_get_dispatch_layout",
+            "ep_layout_single_launch_fits", "ep_layout_auto_single_launch",
+            "ep_get_dispatch_layout_path",
             "ep_get_dispatch_layout_noalloc", "ep_layout_total_rows", "ep_dispatch",
             "ep_combine", "ep_ll_workspace_bytes", "ep_ll_get_dispatch_layout",
             "ep_ll_dispatch", "ep_ll_combine", "ep_debug_set_combine_stall")
@@ -60,6 +65,12 @@ def load(path: str | None = None) -> C.CDLL:
     L.ep_workspace_bytes.argtypes = [i64, i32, i32]
     L.ep_workspace_bytes.restype = sz
     L.ep_get_dispatch_layout.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
+    L.ep_layout_single_launch_fits.argtypes = [i64, i32, i32]
+    L.ep_layout_single_launch_fits.restype = i32
+    L.ep_layout_auto_single_launch.argtypes = [i64, i32, i32]
+    L.ep_layout_auto_single_launch.restype = i32
+    L.ep_get_dispatch_layout_path.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P, P, P, sz,
+                                              i32, P]
     L.ep_layout_total_rows.argtypes = [P, i32, P, P]
     L.ep_dispatch.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, i64, i32, P, P, P, P, P,
                               P, P, P]
@@ -71,7 +82,8 @@ def load(path: str | None = None) -> C.CDLL:
     L.ep_ll_get_dispatch_layout.argtypes = [P, i64, i32, i32, i32, i64, P, P, P, P, P, sz, P]
     L.ep_ll_dispatch.argtypes = [P, i32, i64, i32, P, i64, i32, P, P, P, P, P]
     L.ep_ll_combine.argtypes = [P, i32, P, i64, i32, P, P, P, P]
-    for name in ("ep_get_dispatch_layout", "ep_layout_total_rows", "ep_dispatch", "ep_combine",
+    for name in ("ep_get_dispatch_layout", "ep_get_dispatch_layout_path",
+                 "ep_layout_total_rows", "ep_dispatch", "ep_combine",
                  "ep_ll_get_dispatch_layout", "ep_ll_dispatch", "ep_ll_combine"):
         getattr(L, name).restype = i32
     _lib = L
@@ -128,8 +140,20 @@ def workspace_bytes(num_tokens: int, num_ranks: int, num_experts: int) -> int:
     return int(lib().ep_workspace_bytes(num_tokens, num_ranks, num_experts))
 
 
+def single_launch_fits(num_tokens: int, num_ranks: int, num_experts: int) -> bool:
+    """True if the one-launch (thread-block cluster) layout applies."""
+    return bool(lib().ep_layout_single_launch_fits(num_tokens, num_ranks, num_experts))
+
+
+def auto_single_launch(num_tokens: int, num_ranks: int, num_experts: int) -> bool:
+    """True if path="auto" takes the one-launch layout for this batch."""
+    return bool(lib().ep_layout_auto_single_launch(num_tokens, num_ranks, num_experts))
+
+
 def alloc_layout(num_tokens: int, num_experts: int, num_ranks: int,
                  device: torch.device) -> Layout:
+    """Output tensors and the multi-launch workspace (allocated for every size,
+    so that the same Layout serves either path)."""
     T, R, E = num_tokens, num_ranks, num_experts
     i32 = dict(dtype=torch.int32, device=device)
     ws = torch.empty(max(workspace_bytes(T, R, E), 16), dtype=torch.uint8, device=device)
@@ -139,22 +163,31 @@ def alloc_layout(num_tokens: int, num_experts: int, num_ranks: int,
 
 
 def get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int, *,
-                        err: torch.Tensor | None = None, out: Layout | None = None) -> Layout:
+                        err: torch.Tensor | None = None, out: Layout | None = None,
+                        path: str = "auto") -> Layout:
     """Per-rank / per-expert counts, is_token_in_rank and the slot of every
-    (token, destination rank) pair.  Enqueued on the current stream."""
+    (token, destination rank) pair.  Enqueued on the current stream.
+    path: "auto", "multi" (multi-launch) or "single" (one cluster launch,
+    small batches only); all give the same outputs."""
     _need(topk_idx, "topk_idx", torch.int64)
     if topk_idx.dim() != 2:
         raise EPError("topk_idx must be [num_tokens, num_topk]")
+    if path not in LAYOUT_PATHS:
+        raise EPError(f"path must be one of {sorted(LAYOUT_PATHS)}")
     T, K = topk_idx.shape
     L = out if out is not None else alloc_layout(T, num_experts, num_ranks, topk_idx.device)
     if err is not None:
         _need(err, "err", torch.int32)
-    _check(lib().ep_get_dispatch_layout(
-        _ptr(topk_idx), T, K, num_experts, num_ranks, _ptr(L.num_tokens_per_rank),
-        _ptr(L.num_tokens_per_expert), _ptr(L.is_token_in_rank), _ptr(L.slot),
-        _ptr(L.recv_base), _ptr(err), _ptr(L.workspace),
-        L.workspace.numel() if L.workspace is not None else 0, _stream(topk_idx.device)),
-        "ep_get_dispatch_layout")
+    args = (_ptr(topk_idx), T, K, num_experts, num_ranks, _ptr(L.num_tokens_per_rank),
+            _ptr(L.num_tokens_per_expert), _ptr(L.is_token_in_rank), _ptr(L.slot),
+            _ptr(L.recv_base), _ptr(err), _ptr(L.workspace),
+            L.workspace.numel() if L.workspace is not None else 0)
+    stream = _stream(topk_idx.device)
+    if path == "auto":
+        _check(lib().ep_get_dispatch_layout(*args, stream), "ep_get_dispatch_layout")
+    else:
+        _check(lib().ep_get_dispatch_layout_path(*args, LAYOUT_PATHS[path], stream),
+               "ep_get_dispatch_layout_path")
     return L
 
 

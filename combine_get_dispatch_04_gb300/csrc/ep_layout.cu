@@ -77,10 +77,10 @@ Workspace carve(const Geom& g, void* base) {
 __device__ __forceinline__ void write_member_row(uint8_t* row, uint64_t mask, int R) {
   if ((R & 3) == 0) {
     for (int r = 0; r < R; r += 4) {
-      uint32_t w = (uint32_t)((mask >> r) & 1) | ((uint32_t)((mask >> (r + 1)) & 1) << 8) |
-                   ((uint32_t)((mask >> (r + 2)) & 1) << 16) |
-                   ((uint32_t)((mask >> (r + 3)) & 1) << 24);
-      *reinterpret_cast<uint32_t*>(row + r) = w;
+      // bits r..r+3 spread to the low bit of four bytes: x * 0x00204081 puts
+      // copies of x at bit offsets 0, 7, 14 and 21
+      const uint32_t x = (uint32_t)(mask >> r) & 0xFu;
+      *reinterpret_cast<uint32_t*>(row + r) = (x * 0x00204081u) & 0x01010101u;
     }
   } else {
     for (int r = 0; r < R; ++r) row[r] = (uint8_t)((mask >> r) & 1);
@@ -326,6 +326,314 @@ __global__ void __launch_bounds__(kTok)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Single-launch layout for small batches (decode-size inputs).
+//
+// At these sizes the launches above are bound by latency (each warp's chain
+// of dependent instructions, and the round trips between kernels), not by
+// bytes.  Here one thread-block cluster does the whole layout in one launch,
+// with no scratch memory:
+//   - CTA c of the cluster owns tokens [c*Tc, (c+1)*Tc), Tc = chunks*256,
+//     one token per thread and chunk.  It keeps its tokens' rank masks and
+//     its warps' destination ballots, and counts into its own shared memory:
+//     slots per (source, expert) and tokens per (source, destination).
+//     The chunk loops are not unrolled: the kernel runs once per launch with
+//     a cold instruction cache, so its code size is part of its latency.
+//   - After one cluster barrier every CTA reads the others' counts through
+//     distributed shared memory: the destination totals of the CTAs before
+//     it give its first row in every destination, and the CTA in which a
+//     source rank's tokens start sums that source's rows of
+//     num_tokens_per_rank and num_tokens_per_expert.
+//   - Slots then follow from the stored ballots, chunk by chunk.  A second
+//     cluster barrier, waited on only at the end, keeps every CTA's shared
+//     memory alive until the other CTAs have read it.
+// ---------------------------------------------------------------------------
+constexpr int kCThreads = 256;  // tokens per CTA and chunk
+constexpr int kCWarps = kCThreads / 32;
+constexpr int kCMaxCtas = 16;   // cluster size (above 8 where the device allows it)
+constexpr int kCMaxChunks = 8;  // chunks per CTA
+constexpr int kCMaxTokens = 8 * kCMaxChunks * kCThreads;  // what a cluster of 8 CTAs takes
+constexpr int kCMaxHist = 16384;  // R * E counters of the per-(source, expert) histogram
+
+bool single_launch_fits(int64_t T, int R, int E) {
+  return T > 0 && T <= kCMaxTokens && (int64_t)R * E <= kCMaxHist;
+}
+
+// Largest batch for which EP_LAYOUT_AUTO takes the single launch.  Measured
+// on GB300 (inside the layout -> dispatch -> combine step): 14.1 us against
+// 17.8 us for the multi-launch form at 4096 tokens (32 ranks, 256 experts,
+// top-8); 22.0 us against 18.8 us at 16384 tokens (8 ranks, 256 experts,
+// top-8), where one cluster's 16 SMs have too many tokens each.
+constexpr int kCAutoMaxTokens = 8192;
+
+struct ClusterShape {
+  int ctas;    // CTAs of the one cluster (= the grid)
+  int chunks;  // 256-token chunks per CTA
+};
+
+// As many CTAs as the tokens fill (at most max_ctas), then as few chunks per
+// CTA as that allows.
+ClusterShape cluster_shape(int64_t T, int max_ctas) {
+  const int64_t per_chunk = (int64_t)max_ctas * kCThreads;
+  const int chunks = (int)((T + per_chunk - 1) / per_chunk);
+  const int64_t tc = (int64_t)chunks * kCThreads;
+  return {(int)((T + tc - 1) / tc), chunks};
+}
+
+size_t cluster_smem_bytes(const Geom& g, int chunks) {
+  return sizeof(uint64_t) * (size_t)chunks * kCThreads +
+         sizeof(int32_t) * ((size_t)g.R * g.E + (size_t)g.R * g.R + 2 * (size_t)g.R +
+                            (size_t)kCWarps * g.R + (size_t)chunks * kCWarps * g.R);
+}
+constexpr size_t kCMaxSmem = sizeof(uint64_t) * kCMaxChunks * kCThreads +
+                             sizeof(int32_t) * ((size_t)kCMaxHist + EP_MAX_RANKS * EP_MAX_RANKS +
+                                                2 * EP_MAX_RANKS + kCWarps * EP_MAX_RANKS +
+                                                (size_t)kCMaxChunks * kCWarps * EP_MAX_RANKS);
+
+// floor(e / El) as (e * el_mul) >> 24 with el_mul = ceil(2^24 / El): exact
+// because e * El < 2^24 (both below EP_MAX_EXPERTS = 4096).
+inline uint32_t expert_rank_mul(int El) { return (uint32_t)(((1u << 24) + El - 1) / El); }
+
+__global__ void __launch_bounds__(kCThreads, 1)
+    layout_cluster_kernel(const int64_t* __restrict__ topk_idx, Geom g, int chunks,
+                          uint32_t el_mul, uint8_t* __restrict__ is_token_in_rank,
+                          int32_t* __restrict__ slot, int32_t* __restrict__ ntpr,
+                          int32_t* __restrict__ ntpe, int32_t* __restrict__ recv_base,
+                          int32_t* err) {
+  pdl_wait_then_release();
+  extern __shared__ uint64_t smem64[];
+  const int R = g.R, E = g.E, K = g.K;
+  const int Tr = (int)g.Tr, T = (int)g.T;  // T <= kCMaxTokens
+  uint64_t* msk = smem64;          // [chunks][kCThreads] rank masks of this CTA's tokens
+  int32_t* smem = reinterpret_cast<int32_t*>(msk + chunks * kCThreads);
+  int32_t* hist = smem;            // [R][E]  slots of source s naming expert e
+  int32_t* cnt_sr = hist + R * E;  // [R][R]  tokens of source s sent to r
+  int32_t* tot = cnt_sr + R * R;   // [R]     tokens of this CTA sent to r
+  int32_t* run = tot + R;          // [R]     next row of r for this CTA
+  int32_t* wpre = run + R;         // [kCWarps][R] first row of r for each warp (one chunk)
+  uint32_t* bal = reinterpret_cast<uint32_t*>(wpre + kCWarps * R);  // [chunks][kCWarps][R]
+  const int c = (int)cluster_cta_rank();
+  const int nc = (int)gridDim.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  const int tc = chunks * kCThreads;
+  const int t0 = c * tc;
+  const int t1 = min(T, t0 + tc);  // t0 < t1: the shape leaves no CTA empty
+
+  for (int i = tid; i < R * E + R * R; i += kCThreads) smem[i] = 0;
+  __syncthreads();
+
+  // --- masks, is_token_in_rank, this CTA's counts and its warps' ballots ---
+  bool bad = false;
+#pragma unroll 1
+  for (int j = 0; j < chunks; ++j) {
+    {
+      const int t = t0 + j * kCThreads + tid;
+      const bool valid = t < t1;
+      const int s = valid ? t / Tr : 0;
+      const int64_t* row = topk_idx + (int64_t)t * K;
+      uint64_t mask = 0;
+      for (int k0 = 0; k0 < K; k0 += 8) {
+        int64_t ev[8];  // eight ids loaded before any is used
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ev[u] = (valid && k0 + u < K) ? row[k0 + u] : -1;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int64_t e = ev[u];
+          if (e == -1) continue;
+          if (e < -1 || e >= E) {
+            bad = true;
+          } else {
+            atomicAdd(&hist[s * E + (int)e], 1);
+            mask |= 1ull << (int)(((uint64_t)e * el_mul) >> 24);
+          }
+        }
+      }
+      msk[j * kCThreads + tid] = mask;
+      if (valid) {
+        write_member_row(is_token_in_rank + (int64_t)t * R, mask, R);
+        for (uint64_t m = mask; m != 0; m &= m - 1)
+          atomicAdd(&cnt_sr[s * R + (__ffsll((long long)m) - 1)], 1);
+      }
+      // lane r keeps this warp's ballot of destination r (and of r + 32)
+      uint32_t b0 = 0, b1 = 0;
+      for (int r = 0; r < R; ++r) {
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, (mask >> r) & 1);
+        b0 = r == lane ? b : b0;
+        b1 = r == lane + 32 ? b : b1;
+      }
+      uint32_t* wb = bal + (j * kCWarps + warp) * R;
+      if (lane < R) wb[lane] = b0;
+      if (lane + 32 < R) wb[lane + 32] = b1;
+    }
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && err) atomicOr(err, EP_ERRBIT_BAD_EXPERT);
+  __syncthreads();
+  {
+    const int s_lo = t0 / Tr, s_hi = (t1 - 1) / Tr;
+    for (int r = tid; r < R; r += kCThreads) {
+      int v = 0;
+      for (int s = s_lo; s <= s_hi; ++s) v += cnt_sr[s * R + r];
+      tot[r] = v;
+    }
+  }
+  cluster_arrive();
+  cluster_wait();  // every CTA's counts are final and visible to the cluster
+
+  // --- first row of every destination for this CTA, and recv_base ---
+  if (warp == 0) {
+    // lane l covers destinations l and l + 32; all loads issued before any sum
+    int v[kCMaxCtas][2];
+#pragma unroll
+    for (int cc = 0; cc < kCMaxCtas; ++cc)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = lane + 32 * h;
+        v[cc][h] = (cc < nc && r < R) ? dsmem_ld(dsmem_map(tot + r, (uint32_t)cc)) : 0;
+      }
+    int all[2] = {0, 0}, pre[2] = {0, 0};
+#pragma unroll
+    for (int cc = 0; cc < kCMaxCtas; ++cc)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        all[h] += v[cc][h];
+        pre[h] += cc < c ? v[cc][h] : 0;
+      }
+    int inc0 = all[0], inc1 = all[1];
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a0 = __shfl_up_sync(0xFFFFFFFFu, inc0, o);
+      const int a1 = __shfl_up_sync(0xFFFFFFFFu, inc1, o);
+      if (lane >= o) {
+        inc0 += a0;
+        inc1 += a1;
+      }
+    }
+    const int sum0 = __shfl_sync(0xFFFFFFFFu, inc0, 31);
+    const int sum1 = __shfl_sync(0xFFFFFFFFu, inc1, 31);
+    const int base0 = inc0 - all[0], base1 = sum0 + inc1 - all[1];
+    if (lane < R) run[lane] = base0 + pre[0];
+    if (lane + 32 < R) run[lane + 32] = base1 + pre[1];
+    if (c == 0) {
+      if (lane < R) recv_base[lane] = base0;
+      if (lane + 32 < R) recv_base[lane + 32] = base1;
+      if (lane == 0) recv_base[R] = sum0 + sum1;
+    }
+  }
+
+  // --- rows of num_tokens_per_rank / num_tokens_per_expert of the sources
+  //     whose first token is in this CTA: sums over the CTAs holding them ---
+  {
+    const int s_beg = (t0 + Tr - 1) / Tr, s_end = (t1 + Tr - 1) / Tr;
+    for (int s = s_beg; s < s_end; ++s) {
+      const int c_last = ((s + 1) * Tr - 1) / tc;
+      for (int col = tid; col < R + E; col += kCThreads) {
+        const int32_t* p = col < R ? cnt_sr + s * R + col : hist + s * E + (col - R);
+        int v = 0;
+        for (int cc = c; cc <= c_last; ++cc) v += dsmem_ld(dsmem_map(p, (uint32_t)cc));
+        if (col < R)
+          ntpr[s * R + col] = v;
+        else
+          ntpe[s * E + (col - R)] = v;
+      }
+    }
+  }
+  cluster_arrive();  // this CTA no longer reads the other CTAs' shared memory
+  __syncthreads();   // run[] is written
+
+  // --- slots, chunk by chunk in token order ---
+#pragma unroll 1
+  for (int j = 0; j < chunks; ++j) {
+    {
+      const uint32_t* jb = bal + j * kCWarps * R;
+      for (int r = tid; r < R; r += kCThreads) {  // exclusive prefix over the warps
+        int acc = run[r];
+#pragma unroll
+        for (int w = 0; w < kCWarps; ++w) {
+          wpre[w * R + r] = acc;
+          acc += __popc(jb[w * R + r]);
+        }
+        run[r] = acc;
+      }
+      __syncthreads();
+      const uint64_t mask = msk[j * kCThreads + tid];
+      const int t = t0 + j * kCThreads + tid;
+      if (t < t1) {
+        const uint32_t* mb = jb + warp * R;  // same address for the whole warp
+        const int32_t* mp = wpre + warp * R;
+        int32_t* dst = slot + (int64_t)t * R;
+        if ((R & 3) == 0) {
+          for (int r = 0; r < R; r += 4) {
+            int sv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              sv[i] = ((mask >> (r + i)) & 1) ? mp[r + i] + __popc(mb[r + i] & lt) : -1;
+            *reinterpret_cast<int4*>(dst + r) = make_int4(sv[0], sv[1], sv[2], sv[3]);
+          }
+        } else {
+          for (int r = 0; r < R; ++r)
+            dst[r] = ((mask >> r) & 1) ? mp[r] + __popc(mb[r] & lt) : -1;
+        }
+      }
+      __syncthreads();  // wpre is rewritten for the next chunk
+    }
+  }
+  cluster_wait();  // the other CTAs have finished reading this CTA's shared memory
+}
+
+constexpr int kClusterMaxDevices = 64;
+std::mutex g_cluster_mu;
+int g_cluster_ctas[kClusterMaxDevices] = {};  // largest usable cluster per device, 0 = unknown
+
+// One-time set-up per device: the kernel's shared-memory limit, and whether
+// a cluster of 16 CTAs (a non-portable size) can be scheduled; otherwise 8.
+cudaError_t cluster_max_ctas(int* out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kClusterMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_cluster_mu);
+  if (g_cluster_ctas[dev] == 0) {
+    e = cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kCMaxSmem);
+    if (e != cudaSuccess) return e;
+    int ctas = 8;
+    if (cudaFuncSetAttribute(layout_cluster_kernel,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(kCMaxCtas);
+      cfg.blockDim = dim3(kCThreads);
+      cfg.dynamicSmemBytes = kCMaxSmem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kCMaxCtas;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, layout_cluster_kernel, &cfg) == cudaSuccess && n > 0)
+        ctas = kCMaxCtas;
+    }
+    cudaGetLastError();  // a refused non-portable size is not an error of the caller's
+    g_cluster_ctas[dev] = ctas;
+  }
+  *out = g_cluster_ctas[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_layout_cluster(const int64_t* topk_idx, const Geom& g, int32_t* ntpr,
+                                  int32_t* ntpe, uint8_t* is_token_in_rank, int32_t* slot,
+                                  int32_t* recv_base, int32_t* err_word, cudaStream_t st) {
+  int max_ctas = 8;
+  const cudaError_t e = cluster_max_ctas(&max_ctas);
+  if (e != cudaSuccess) return e;
+  const ClusterShape cs = cluster_shape(g.T, max_ctas);
+  return launch_pdl_cluster(layout_cluster_kernel, cs.ctas, kCThreads,
+                            cluster_smem_bytes(g, cs.chunks), cs.ctas, st, topk_idx, g,
+                            cs.chunks, expert_rank_mul(g.El), is_token_in_rank, slot, ntpr,
+                            ntpe, recv_base, err_word);
+}
+
 // The layout's launches on one stream, given carved scratch.
 void launch_layout(const int64_t* topk_idx, const Geom& g, const Workspace& ws,
                    int32_t* ntpr, int32_t* ntpe, uint8_t* is_token_in_rank, int32_t* slot,
@@ -351,6 +659,52 @@ extern "C" size_t ep_workspace_bytes(int64_t num_tokens, int num_ranks, int num_
   return carve(g, nullptr).bytes;
 }
 
+extern "C" int ep_layout_single_launch_fits(int64_t num_tokens, int num_ranks, int num_experts) {
+  if (!routing_ok(num_tokens, 1, num_experts, num_ranks)) return 0;
+  return single_launch_fits(num_tokens, num_ranks, num_experts) ? 1 : 0;
+}
+
+extern "C" int ep_layout_auto_single_launch(int64_t num_tokens, int num_ranks, int num_experts) {
+  return ep_layout_single_launch_fits(num_tokens, num_ranks, num_experts) &&
+         num_tokens <= kCAutoMaxTokens;
+}
+
+extern "C" ep_status_t ep_get_dispatch_layout_path(
+    const int64_t* topk_idx, int64_t num_tokens, int num_topk, int num_experts, int num_ranks,
+    int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+    int32_t* slot, int32_t* recv_base, int32_t* err_word, void* workspace,
+    size_t workspace_bytes, int path, ep_stream_t stream) {
+  if (!routing_ok(num_tokens, num_topk, num_experts, num_ranks)) return EP_ERR_INVALID_ARG;
+  if (!num_tokens_per_rank || !num_tokens_per_expert || !recv_base) return EP_ERR_INVALID_ARG;
+  if (path != EP_LAYOUT_AUTO && path != EP_LAYOUT_MULTI_LAUNCH && path != EP_LAYOUT_SINGLE_LAUNCH)
+    return EP_ERR_INVALID_ARG;
+  const bool fits = single_launch_fits(num_tokens, num_ranks, num_experts);
+  if (path == EP_LAYOUT_SINGLE_LAUNCH && !fits) return EP_ERR_INVALID_ARG;
+  const bool single = path == EP_LAYOUT_SINGLE_LAUNCH ||
+                      (path == EP_LAYOUT_AUTO && fits && num_tokens <= kCAutoMaxTokens);
+  if (num_tokens > 0) {
+    if (!topk_idx || !is_token_in_rank || !slot) return EP_ERR_INVALID_ARG;
+    if (!aligned16(slot) || !aligned16(is_token_in_rank) || !aligned16(topk_idx))
+      return EP_ERR_INVALID_ARG;
+    if (!single && (!workspace || !aligned16(workspace))) return EP_ERR_INVALID_ARG;
+  }
+  const Geom g = make_geom(num_tokens, num_topk, num_experts, num_ranks);
+  if (single) {
+    if (launch_layout_cluster(topk_idx, g, num_tokens_per_rank, num_tokens_per_expert,
+                              is_token_in_rank, slot, recv_base, err_word,
+                              to_cuda(stream)) != cudaSuccess) {
+      cudaGetLastError();  // clear the launch error; the status reports it
+      return EP_ERR_CUDA;
+    }
+    return EP_OK;
+  }
+  const Workspace ws = carve(g, workspace);
+  if (num_tokens > 0 && workspace_bytes < ws.bytes) return EP_ERR_CAPACITY;
+  launch_layout(topk_idx, g, ws, num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank,
+                slot, recv_base, err_word, to_cuda(stream));
+  return launch_status();
+}
+
 extern "C" ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t num_tokens,
                                               int num_topk, int num_experts, int num_ranks,
                                               int32_t* num_tokens_per_rank,
@@ -359,20 +713,10 @@ extern "C" ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t n
                                               int32_t* recv_base, int32_t* err_word,
                                               void* workspace, size_t workspace_bytes,
                                               ep_stream_t stream) {
-  if (!routing_ok(num_tokens, num_topk, num_experts, num_ranks)) return EP_ERR_INVALID_ARG;
-  if (!num_tokens_per_rank || !num_tokens_per_expert || !recv_base) return EP_ERR_INVALID_ARG;
-  if (num_tokens > 0) {
-    if (!topk_idx || !is_token_in_rank || !slot || !workspace) return EP_ERR_INVALID_ARG;
-    if (!aligned16(slot) || !aligned16(is_token_in_rank) || !aligned16(workspace) ||
-        !aligned16(topk_idx))
-      return EP_ERR_INVALID_ARG;
-  }
-  const Geom g = make_geom(num_tokens, num_topk, num_experts, num_ranks);
-  const Workspace ws = carve(g, workspace);
-  if (num_tokens > 0 && workspace_bytes < ws.bytes) return EP_ERR_CAPACITY;
-  launch_layout(topk_idx, g, ws, num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank,
-                slot, recv_base, err_word, to_cuda(stream));
-  return launch_status();
+  return ep_get_dispatch_layout_path(topk_idx, num_tokens, num_topk, num_experts, num_ranks,
+                                     num_tokens_per_rank, num_tokens_per_expert,
+                                     is_token_in_rank, slot, recv_base, err_word, workspace,
+                                     workspace_bytes, EP_LAYOUT_AUTO, stream);
 }
 
 extern "C" ep_status_t ep_layout_total_rows(const int32_t* recv_base, int num_ranks,

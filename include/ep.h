@@ -98,14 +98,61 @@ size_t ep_workspace_bytes(int64_t num_tokens, int num_ranks, int num_experts);
  * err_word (device, nullable): EP_ERRBIT_BAD_EXPERT if some id is outside
  *   [-1, E) (the slot is then treated as masked).
  * workspace (device): at least ep_workspace_bytes(T, R, E) bytes, passed as
- *   workspace_bytes; a smaller value returns EP_ERR_CAPACITY.
+ *   workspace_bytes; a smaller value returns EP_ERR_CAPACITY.  Unused (may be
+ *   NULL, with workspace_bytes 0) when ep_layout_auto_single_launch(T, R, E):
+ *   such batches take the single-launch form described below.
  * T = 0 is valid (counts and recv_base are zeroed).
+ * Same as ep_get_dispatch_layout_path(..., EP_LAYOUT_AUTO, stream).
  */
 ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t num_tokens, int num_topk,
                                    int num_experts, int num_ranks, int32_t* num_tokens_per_rank,
                                    int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
                                    int32_t* slot, int32_t* recv_base, int32_t* err_word,
                                    void* workspace, size_t workspace_bytes, ep_stream_t stream);
+
+/*
+ * Which kernels compute the layout.  Both forms give identical outputs.
+ *
+ * EP_LAYOUT_MULTI_LAUNCH: two or three launches spread over the whole GPU
+ *   (counts per block of tokens, block offsets, slots), with scratch in the
+ *   caller's workspace.  Any size.
+ * EP_LAYOUT_SINGLE_LAUNCH: one launch of one thread-block cluster of up to
+ *   16 CTAs (8 where the device does not schedule 16), which exchange their
+ *   counts through distributed shared memory; no workspace.  For small
+ *   batches only (ep_layout_single_launch_fits): T <= 16384 and
+ *   R * E <= 16384.  At decode sizes the layout is bound by latency, and
+ *   this form removes the round trips between kernels.  The pages run layout, count exchange (notify_dispatch,
+ *   cached_notify) and data movement as separate kernels ("Scope",
+ *   Internode HT); this fused form has no counterpart there.
+ * EP_LAYOUT_AUTO: the single-launch form where it is the faster one
+ *   (ep_layout_auto_single_launch: it fits and T <= 8192), else multi-launch.
+ */
+typedef enum {
+  EP_LAYOUT_AUTO = 0,
+  EP_LAYOUT_MULTI_LAUNCH = 1,
+  EP_LAYOUT_SINGLE_LAUNCH = 2
+} ep_layout_path_t;
+
+/* 1 if the single-launch form applies to (T, R, E), else 0 (also for invalid sizes). */
+int ep_layout_single_launch_fits(int64_t num_tokens, int num_ranks, int num_experts);
+
+/* 1 if EP_LAYOUT_AUTO takes the single-launch form for (T, R, E), else 0. */
+int ep_layout_auto_single_launch(int64_t num_tokens, int num_ranks, int num_experts);
+
+/*
+ * ep_get_dispatch_layout with an explicit choice of kernels (`path`, an
+ * ep_layout_path_t).  Arguments and outputs as ep_get_dispatch_layout.
+ * Returns EP_ERR_INVALID_ARG, with nothing enqueued, for an unknown path or
+ * for EP_LAYOUT_SINGLE_LAUNCH when the batch does not fit it (T = 0
+ * included).  The workspace is needed only when the multi-launch form runs.
+ */
+ep_status_t ep_get_dispatch_layout_path(const int64_t* topk_idx, int64_t num_tokens,
+                                        int num_topk, int num_experts, int num_ranks,
+                                        int32_t* num_tokens_per_rank,
+                                        int32_t* num_tokens_per_expert,
+                                        uint8_t* is_token_in_rank, int32_t* slot,
+                                        int32_t* recv_base, int32_t* err_word, void* workspace,
+                                        size_t workspace_bytes, int path, ep_stream_t stream);
 
 /*
  * The same layout as ep_get_dispatch_layout, for callers that cannot

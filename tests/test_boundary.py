@@ -64,6 +64,12 @@ def _layout_call(eplib, T=8, K=2, E=8, R=2, ptrs=True, ws_bytes=1 << 20):
     return eplib.ep_get_dispatch_layout(p, T, K, E, R, p, p, p, p, p, None, p, ws_bytes, None)
 
 
+def _layout_path_call(eplib, path, T=8, K=2, E=8, R=2):
+    p = C.c_void_p(16)  # never dereferenced: the checks fail first
+    return eplib.ep_get_dispatch_layout_path(p, T, K, E, R, p, p, p, p, p, None, p, 1 << 20,
+                                             path, None)
+
+
 def test_layout_rejects_bad_arguments(eplib):
     assert _layout_call(eplib, E=7) == EP_ERR_INVALID_ARG        # E % R
     assert _layout_call(eplib, T=9) == EP_ERR_INVALID_ARG        # T % R
@@ -71,7 +77,36 @@ def test_layout_rejects_bad_arguments(eplib):
     assert _layout_call(eplib, K=33) == EP_ERR_INVALID_ARG       # above EP_MAX_TOPK
     assert _layout_call(eplib, R=65, E=65 * 2, T=130) == EP_ERR_INVALID_ARG
     assert _layout_call(eplib, ptrs=False) == EP_ERR_INVALID_ARG
-    assert _layout_call(eplib, ws_bytes=8) == EP_ERR_CAPACITY    # workspace too small
+    # workspace too small (a batch too large for the single-launch form, which needs none)
+    assert not eplib.ep_layout_single_launch_fits(40000, 2, 8)
+    assert _layout_call(eplib, T=40000, ws_bytes=8) == EP_ERR_CAPACITY
+
+
+def test_single_launch_layout_limits(eplib):
+    fits = eplib.ep_layout_single_launch_fits
+    assert fits(4096, 32, 256) == 1       # decode: 32 ranks x 128 tokens, 256 experts
+    assert fits(16384, 8, 256) == 1       # 8 CTAs x 8 chunks x 256 tokens
+    assert fits(512, 4, 16) == 1
+    assert fits(16386, 2, 8) == 0         # more tokens than one cluster holds
+    assert fits(32768, 8, 256) == 0
+    assert fits(131072, 16, 64) == 0
+    assert fits(512, 64, 512) == 0        # R * E above the shared-memory histogram
+    assert fits(0, 4, 16) == 0            # T = 0 takes the multi-launch form
+    assert fits(10, 4, 16) == 0           # invalid sizes
+    auto = eplib.ep_layout_auto_single_launch
+    assert auto(4096, 32, 256) == 1 and auto(8192, 8, 256) == 1
+    assert auto(16384, 8, 256) == 0       # fits, but the multi-launch form is faster there
+    assert auto(512, 64, 512) == 0
+
+
+def test_layout_path_rejects_bad_arguments(eplib):
+    AUTO, MULTI, SINGLE = 0, 1, 2
+    assert _layout_path_call(eplib, 3) == EP_ERR_INVALID_ARG     # unknown path
+    assert _layout_path_call(eplib, -1) == EP_ERR_INVALID_ARG
+    assert _layout_path_call(eplib, SINGLE, T=40000) == EP_ERR_INVALID_ARG  # does not fit
+    assert _layout_path_call(eplib, SINGLE, T=0) == EP_ERR_INVALID_ARG
+    assert _layout_path_call(eplib, MULTI, E=7) == EP_ERR_INVALID_ARG
+    assert _layout_path_call(eplib, AUTO, T=9) == EP_ERR_INVALID_ARG
 
 
 def test_dispatch_rejects_bad_arguments(eplib):

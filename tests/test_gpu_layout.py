@@ -1,6 +1,8 @@
 """GPU parity: ep_get_dispatch_layout against the CPU oracle, bit-exact on
 every output (counts, is_token_in_rank, slot, recv_base), on small and ragged
-cases, the extremes, and all five workloads at full size."""
+cases, the extremes, and all five workloads at full size.  Both kernel paths
+are checked: the multi-launch form and the single-launch (one thread-block
+cluster) form for the batches it takes."""
 from __future__ import annotations
 
 import numpy as np
@@ -9,7 +11,7 @@ import torch
 
 import oracle
 from ep_testlib import device_inputs, full_case, small_configs
-from workloads import CONFIGS, make_case
+from workloads import CONFIGS, Config, make_case
 
 pytestmark = pytest.mark.gpu
 
@@ -33,27 +35,80 @@ def poison_layout(L):
         L.workspace.fill_(0xCD)
 
 
-@pytest.mark.parametrize("cfg", small_configs(), ids=lambda c: c.name)
-def test_layout_small(ep, cfg):
-    c = make_case(cfg, with_hidden=False)
-    idx, _, _ = device_inputs(c)
+PATHS = ["multi", "single"]
+
+
+def layout_on(ep, idx, cfg, path, err=None):
+    """The layout on the given path, poisoned first; None (after checking
+    that the call is refused on the host) when the single-launch form does
+    not take this batch."""
     L = ep.alloc_layout(cfg.num_tokens, cfg.num_experts, cfg.num_ranks, idx.device)
     poison_layout(L)
+    if path == "single" and not ep.single_launch_fits(cfg.num_tokens, cfg.num_ranks,
+                                                      cfg.num_experts):
+        with pytest.raises(ep.EPError):
+            ep.get_dispatch_layout(idx, cfg.num_experts, cfg.num_ranks, out=L, path=path)
+        return None
+    ep.get_dispatch_layout(idx, cfg.num_experts, cfg.num_ranks, err=err, out=L, path=path)
+    return L
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("cfg", small_configs(), ids=lambda c: c.name)
+def test_layout_small(ep, cfg, path):
+    c = make_case(cfg, with_hidden=False)
+    idx, _, _ = device_inputs(c)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ep.get_dispatch_layout(idx, cfg.num_experts, cfg.num_ranks, err=err, out=L)
+    L = layout_on(ep, idx, cfg, path, err)
+    if L is None:
+        return
     want = oracle.layout(c.topk_idx, cfg.num_experts, cfg.num_ranks)
     compare_layout(L, want)
     assert int(err.item()) == 0
     assert ep.total_rows(L) == want.num_rows
 
 
+def single_launch_configs():
+    """Shapes that drive the single-launch form through several CTAs and
+    chunks, ragged last CTAs and chunks, sources spread over several CTAs,
+    warps holding many sources, and the largest histogram it takes."""
+    specs = [  # name, R, T_r, E, K, routing, mask
+        ("s_r3_ragged", 3, 5000, 12, 4, "zipf", 0.05),     # several chunks, last CTA ragged
+        ("s_r7_16380", 7, 2340, 14, 2, "uniform", 0.0),    # four tokens short of the maximum
+        ("s_r2_16384", 2, 8192, 8, 6, "zipf", 0.1),        # exactly the maximum
+        ("s_r64_tr1", 64, 1, 128, 8, "uniform", 0.0),      # every lane its own source
+        ("s_r64_e256", 64, 100, 256, 8, "zipf", 0.05),     # R * E = 16384
+        ("s_r5_k32", 5, 1500, 40, 32, "uniform", 0.3),     # four batches of ids per token
+        ("s_r16_1000", 16, 1000, 64, 6, "zipf", 0.05),     # sources straddle CTAs
+        ("s_r3_tr5", 3, 5, 6, 2, "uniform", 0.0),          # one CTA, 15 tokens
+    ]
+    return [Config(n, R, Tr, 8, E, K, routing=rt, zipf_s=1.2 if rt == "zipf" else 0.0,
+                   mask_prob=m, seed=950 + i)
+            for i, (n, R, Tr, E, K, rt, m) in enumerate(specs)]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("cfg", single_launch_configs(), ids=lambda c: c.name)
+def test_layout_single_launch_shapes(ep, cfg, path):
+    assert ep.single_launch_fits(cfg.num_tokens, cfg.num_ranks, cfg.num_experts)
+    c = make_case(cfg, with_hidden=False)
+    idx, _, _ = device_inputs(c)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L = layout_on(ep, idx, cfg, path, err)
+    compare_layout(L, oracle.layout(c.topk_idx, cfg.num_experts, cfg.num_ranks))
+    assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("path", ["auto"] + PATHS)
 @pytest.mark.parametrize("name", list(CONFIGS))
-def test_layout_full_size(ep, name):
+def test_layout_full_size(ep, name, path):
     cfg = CONFIGS[name]
     c, want = full_case(name)
     idx, _, _ = device_inputs(type(c)(c.cfg, c.topk_idx, c.topk_weights, None))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    L = ep.get_dispatch_layout(idx, cfg.num_experts, cfg.num_ranks, err=err)
+    L = layout_on(ep, idx, cfg, path, err)
+    if L is None:
+        return
     compare_layout(L, want)
     assert int(err.item()) == 0
 
@@ -70,7 +125,8 @@ def test_layout_repeated_calls_reuse_buffers(ep):
         compare_layout(L, oracle.layout(c.topk_idx, cfg.num_experts, cfg.num_ranks))
 
 
-def test_layout_out_of_range_ids_are_flagged_and_masked(ep):
+@pytest.mark.parametrize("path", PATHS)
+def test_layout_out_of_range_ids_are_flagged_and_masked(ep, path):
     cfg = CONFIGS["tiny"]
     c = make_case(cfg, with_hidden=False)
     idx_np = c.topk_idx.copy()
@@ -79,7 +135,7 @@ def test_layout_out_of_range_ids_are_flagged_and_masked(ep):
     idx_np[511, 3] = 1 << 40
     idx = torch.from_numpy(idx_np).cuda()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    L = ep.get_dispatch_layout(idx, cfg.num_experts, cfg.num_ranks, err=err)
+    L = layout_on(ep, idx, cfg, path, err)
     want = oracle.layout(idx_np, cfg.num_experts, cfg.num_ranks)
     assert want.err_bits == 1
     compare_layout(L, want)

@@ -342,7 +342,7 @@ def run_ours(args, cfg: Config):
         DL = None
 
         def do_layout():
-            ep.ll_get_dispatch_layout(idx, E, R, err=err, out=LL)
+            ep.ll_get_dispatch_layout(idx, E, R, err=err, out=LL, path=args.layout_kernels)
 
         def do_dispatch(a, b):
             LLc = LL if (a, b) == (0, T) else _replace(LL, ll_slot=LL.ll_slot[a:b])
@@ -502,7 +502,11 @@ def run_ours(args, cfg: Config):
 
     layout_kernels = None
     if args.layout == "ll":
-        layout_launches = 3  # rank, expert scan, assign
+        if args.layout_kernels == "single" or (args.layout_kernels == "auto"
+                                               and ep.ll_auto_single_launch(T, K, R, E)):
+            layout_launches, layout_kernels = 1, "single"
+        else:
+            layout_launches, layout_kernels = 3, "multi"  # rank, expert scan, assign
     elif args.layout_kernels == "single" or (args.layout_kernels == "auto"
                                              and ep.auto_single_launch(T, R, E)):
         layout_launches, layout_kernels = 1, "single"  # one thread-block cluster
@@ -568,8 +572,8 @@ def main(argv=None):
     ap.add_argument("--layout", choices=["ht", "ll"], default="ht",
                     help="receive layout: rank-major (ht, default) or expert-major (ll)")
     ap.add_argument("--layout-kernels", choices=["auto", "multi", "single"], default="auto",
-                    help="rank-major layout kernels: one cluster launch (single, small "
-                         "batches), the multi-launch form, or the library's choice (auto)")
+                    help="layout kernels: one cluster launch (single, small batches), the "
+                         "multi-launch form, or the library's choice (auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="token chunks the end-to-end step pipelines its copies over")

@@ -40,7 +40,9 @@ EXPORTED = ("ep_status_string", "ep_workspace_bytes", "ep_get_dispatch_layout",
             "ep_get_dispatch_layout_path",
             "ep_get_dispatch_layout_noalloc", "ep_layout_total_rows", "ep_dispatch",
             "ep_combine", "ep_ll_workspace_bytes", "ep_ll_get_dispatch_layout",
-            "ep_ll_dispatch", "ep_ll_combine", "ep_debug_set_combine_stall")
+            "ep_ll_dispatch", "ep_ll_combine", "ep_debug_set_combine_stall",
+            "ep_ll_layout_single_launch_fits", "ep_ll_layout_auto_single_launch",
+            "ep_ll_get_dispatch_layout_path")
 
 _lib = None
 
@@ -80,11 +82,17 @@ def load(path: str | None = None) -> C.CDLL:
     L.ep_ll_workspace_bytes.argtypes = [i64, i32, i32]
     L.ep_ll_workspace_bytes.restype = sz
     L.ep_ll_get_dispatch_layout.argtypes = [P, i64, i32, i32, i32, i64, P, P, P, P, P, sz, P]
+    L.ep_ll_get_dispatch_layout_path.argtypes = [P, i64, i32, i32, i32, i64, P, P, P, P, P, sz,
+                                                 i32, P]
+    for name in ("ep_ll_layout_single_launch_fits", "ep_ll_layout_auto_single_launch"):
+        getattr(L, name).argtypes = [i64, i32, i32, i32]
+        getattr(L, name).restype = i32
     L.ep_ll_dispatch.argtypes = [P, i32, i64, i32, P, i64, i32, P, P, P, P, P]
     L.ep_ll_combine.argtypes = [P, i32, P, i64, i32, P, P, P, P]
     for name in ("ep_get_dispatch_layout", "ep_get_dispatch_layout_path",
                  "ep_layout_total_rows", "ep_dispatch", "ep_combine",
-                 "ep_ll_get_dispatch_layout", "ep_ll_dispatch", "ep_ll_combine"):
+                 "ep_ll_get_dispatch_layout", "ep_ll_get_dispatch_layout_path",
+                 "ep_ll_dispatch", "ep_ll_combine"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -314,12 +322,29 @@ def alloc_ll_layout(num_tokens: int, num_topk: int, num_experts: int, num_ranks:
                     num_experts, num_ranks, int(expert_capacity), ws)
 
 
+def ll_single_launch_fits(num_tokens: int, num_topk: int, num_ranks: int,
+                          num_experts: int) -> bool:
+    """True if the one-launch (thread-block cluster) expert-major layout applies."""
+    return bool(lib().ep_ll_layout_single_launch_fits(num_tokens, num_topk, num_ranks,
+                                                      num_experts))
+
+
+def ll_auto_single_launch(num_tokens: int, num_topk: int, num_ranks: int,
+                          num_experts: int) -> bool:
+    """True if path="auto" takes the one-launch expert-major layout."""
+    return bool(lib().ep_ll_layout_auto_single_launch(num_tokens, num_topk, num_ranks,
+                                                      num_experts))
+
+
 def ll_get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int,
                            expert_capacity: int | None = None, *,
                            err: torch.Tensor | None = None,
-                           out: LLLayout | None = None) -> LLLayout:
-    """Rows of the expert-major layout (default capacity: T rows per expert)."""
+                           out: LLLayout | None = None, path: str = "auto") -> LLLayout:
+    """Rows of the expert-major layout (default capacity: T rows per expert).
+    path: "auto", "multi" or "single" (one cluster launch, small batches)."""
     _need(topk_idx, "topk_idx", torch.int64)
+    if path not in LAYOUT_PATHS:
+        raise EPError(f"path must be one of {sorted(LAYOUT_PATHS)}")
     T, K = topk_idx.shape
     if out is not None:
         L = out
@@ -331,10 +356,13 @@ def ll_get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: 
     ws = L.workspace
     if err is not None:
         _need(err, "err", torch.int32)
-    _check(lib().ep_ll_get_dispatch_layout(
-        _ptr(topk_idx), T, K, num_experts, num_ranks, cap, _ptr(L.ll_slot), _ptr(L.ll_count),
-        _ptr(L.ll_src_offset), _ptr(err), _ptr(ws), ws.numel(), _stream(dev)),
-        "ep_ll_get_dispatch_layout")
+    args = (_ptr(topk_idx), T, K, num_experts, num_ranks, cap, _ptr(L.ll_slot),
+            _ptr(L.ll_count), _ptr(L.ll_src_offset), _ptr(err), _ptr(ws), ws.numel())
+    if path == "auto":
+        _check(lib().ep_ll_get_dispatch_layout(*args, _stream(dev)), "ep_ll_get_dispatch_layout")
+    else:
+        _check(lib().ep_ll_get_dispatch_layout_path(*args, LAYOUT_PATHS[path], _stream(dev)),
+               "ep_ll_get_dispatch_layout_path")
     return L
 
 

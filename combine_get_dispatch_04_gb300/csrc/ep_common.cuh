@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "ep.h"
 
 namespace ep {
@@ -85,6 +87,61 @@ inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
+
+// Per-device set-up of a single-cluster kernel, done once by the caller
+// (under its own lock): raises the kernel's dynamic shared-memory limit to
+// `smem`, and returns in *out the largest cluster it can run: 16 CTAs (a
+// non-portable size) when the device schedules a cluster of 16 blocks of
+// `block` threads and `smem` bytes, else 8.
+template <typename... KArgs>
+inline cudaError_t setup_single_cluster(void (*kernel)(KArgs...), int block, size_t smem,
+                                        int* out) {
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int ctas = 8;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n > 0) ctas = 16;
+  }
+  cudaGetLastError();  // a refused non-portable size is not the caller's error
+  *out = ctas;
+  return cudaSuccess;
+}
+
+// Per-device cache of setup_single_cluster's answer for one kernel.
+struct ClusterSizeCache {
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu;
+  int ctas[kMaxDevices] = {};  // 0 = not yet set up
+
+  template <typename... KArgs>
+  cudaError_t get(void (*kernel)(KArgs...), int block, size_t smem, int* out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (ctas[dev] == 0) {
+      e = setup_single_cluster(kernel, block, smem, &ctas[dev]);
+      if (e != cudaSuccess) return e;
+    }
+    *out = ctas[dev];
+    return cudaSuccess;
+  }
+};
 
 // ---------------------------------------------------------------------------
 // device side

@@ -580,52 +580,13 @@ __global__ void __launch_bounds__(kCThreads, 1)
   cluster_wait();  // the other CTAs have finished reading this CTA's shared memory
 }
 
-constexpr int kClusterMaxDevices = 64;
-std::mutex g_cluster_mu;
-int g_cluster_ctas[kClusterMaxDevices] = {};  // largest usable cluster per device, 0 = unknown
-
-// One-time set-up per device: the kernel's shared-memory limit, and whether
-// a cluster of 16 CTAs (a non-portable size) can be scheduled; otherwise 8.
-cudaError_t cluster_max_ctas(int* out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kClusterMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_cluster_mu);
-  if (g_cluster_ctas[dev] == 0) {
-    e = cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kCMaxSmem);
-    if (e != cudaSuccess) return e;
-    int ctas = 8;
-    if (cudaFuncSetAttribute(layout_cluster_kernel,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(kCMaxCtas);
-      cfg.blockDim = dim3(kCThreads);
-      cfg.dynamicSmemBytes = kCMaxSmem;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = kCMaxCtas;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, layout_cluster_kernel, &cfg) == cudaSuccess && n > 0)
-        ctas = kCMaxCtas;
-    }
-    cudaGetLastError();  // a refused non-portable size is not an error of the caller's
-    g_cluster_ctas[dev] = ctas;
-  }
-  *out = g_cluster_ctas[dev];
-  return cudaSuccess;
-}
+ClusterSizeCache g_cluster_size;  // 16 or 8 CTAs, per device
 
 cudaError_t launch_layout_cluster(const int64_t* topk_idx, const Geom& g, int32_t* ntpr,
                                   int32_t* ntpe, uint8_t* is_token_in_rank, int32_t* slot,
                                   int32_t* recv_base, int32_t* err_word, cudaStream_t st) {
   int max_ctas = 8;
-  const cudaError_t e = cluster_max_ctas(&max_ctas);
+  const cudaError_t e = g_cluster_size.get(layout_cluster_kernel, kCThreads, kCMaxSmem, &max_ctas);
   if (e != cudaSuccess) return e;
   const ClusterShape cs = cluster_shape(g.T, max_ctas);
   return launch_pdl_cluster(layout_cluster_kernel, cs.ctas, kCThreads,

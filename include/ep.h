@@ -286,13 +286,43 @@ size_t ep_ll_workspace_bytes(int64_t num_tokens, int num_ranks, int num_experts)
  *   ll_count [E] int32: slots naming each expert, over all sources
  *   ll_src_offset [E, R] int32 (nullable): first row of source s within
  *     expert e's rows (relative to e*cap).
- * workspace: ep_ll_workspace_bytes(T, R, E) bytes (EP_ERR_CAPACITY if less).
+ * workspace: ep_ll_workspace_bytes(T, R, E) bytes (EP_ERR_CAPACITY if less);
+ *   unused (may be NULL) when ep_ll_layout_auto_single_launch(T, K, R, E).
+ * Same as ep_ll_get_dispatch_layout_path(..., EP_LAYOUT_AUTO, stream).
  */
 ep_status_t ep_ll_get_dispatch_layout(const int64_t* topk_idx, int64_t num_tokens, int num_topk,
                                       int num_experts, int num_ranks, int64_t expert_capacity,
                                       int32_t* ll_slot, int32_t* ll_count, int32_t* ll_src_offset,
                                       int32_t* err_word, void* workspace, size_t workspace_bytes,
                                       ep_stream_t stream);
+
+/*
+ * The expert-major layout's kernels, as for the rank-major layout
+ * (ep_layout_path_t):
+ *   EP_LAYOUT_MULTI_LAUNCH: three launches over the whole GPU (ranks within
+ *     128-token chunks, a prefix over chunks per expert, rows), with
+ *     scratch in the caller's workspace.  Any size.
+ *   EP_LAYOUT_SINGLE_LAUNCH: one launch of one thread-block cluster of up to
+ *     16 CTAs that exchange per-expert counts through distributed shared
+ *     memory; no workspace.  Small batches only
+ *     (ep_ll_layout_single_launch_fits): E <= 1024, and every warp of a
+ *     cluster of 8 CTAs walks at most 2048 slots (roughly T * K <= 131072
+ *     when R divides 64).
+ *   EP_LAYOUT_AUTO: the single launch whenever it fits (measured faster
+ *     at every size it takes); ep_ll_layout_auto_single_launch says which.
+ * Both give identical outputs.  EP_LAYOUT_SINGLE_LAUNCH on a batch that does
+ * not fit (T = 0 included) returns EP_ERR_INVALID_ARG with nothing enqueued.
+ */
+int ep_ll_layout_single_launch_fits(int64_t num_tokens, int num_topk, int num_ranks,
+                                    int num_experts);
+int ep_ll_layout_auto_single_launch(int64_t num_tokens, int num_topk, int num_ranks,
+                                    int num_experts);
+ep_status_t ep_ll_get_dispatch_layout_path(const int64_t* topk_idx, int64_t num_tokens,
+                                           int num_topk, int num_experts, int num_ranks,
+                                           int64_t expert_capacity, int32_t* ll_slot,
+                                           int32_t* ll_count, int32_t* ll_src_offset,
+                                           int32_t* err_word, void* workspace,
+                                           size_t workspace_bytes, int path, ep_stream_t stream);
 
 /*
  * Low-latency dispatch: for every slot with ll_slot[t][k] >= 0, row

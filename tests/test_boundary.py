@@ -99,6 +99,38 @@ def test_single_launch_layout_limits(eplib):
     assert auto(512, 64, 512) == 0
 
 
+def test_ll_single_launch_layout_limits(eplib):
+    fits = eplib.ep_ll_layout_single_launch_fits
+    auto = eplib.ep_ll_layout_auto_single_launch
+    assert fits(4096, 8, 32, 256) == 1      # decode: 2 warps of 64 tokens per source at 8 CTAs
+    assert fits(512, 4, 4, 16) == 1
+    assert fits(8192, 16, 1, 16) == 1       # one source: 64 warps of 128 tokens x 16 slots
+    assert fits(8192 + 1, 16, 1, 16) == 0   # a warp would walk more than 2048 slots
+    assert fits(4096, 8, 32, 2048) == 0     # more experts than the per-warp counters hold
+    assert fits(0, 8, 32, 256) == 0
+    assert fits(10, 8, 4, 16) == 0          # invalid sizes
+    assert auto(4096, 8, 32, 256) == 1
+    assert fits(16384, 8, 8, 256) == 1      # 8 warps of 256 tokens per source at 8 CTAs
+    assert auto(16384, 8, 8, 256) == 1      # the single launch wins wherever it fits
+    assert auto(32768, 8, 8, 256) == 0
+    assert fits(32768, 8, 8, 256) == 0      # 4096 slots per warp at 8 CTAs
+
+
+def _ll_path_call(eplib, path, T=8, K=2, E=8, R=2, cap=8):
+    p = C.c_void_p(16)  # never dereferenced: the checks fail first
+    return eplib.ep_ll_get_dispatch_layout_path(p, T, K, E, R, cap, p, p, p, None, p, 1 << 20,
+                                                path, None)
+
+
+def test_ll_layout_path_rejects_bad_arguments(eplib):
+    SINGLE = 2
+    assert _ll_path_call(eplib, 3) == EP_ERR_INVALID_ARG
+    assert _ll_path_call(eplib, SINGLE, T=0) == EP_ERR_INVALID_ARG
+    assert _ll_path_call(eplib, SINGLE, E=2048, R=2) == EP_ERR_INVALID_ARG  # E above 1024
+    assert _ll_path_call(eplib, SINGLE, cap=-1) == EP_ERR_INVALID_ARG
+    assert _ll_path_call(eplib, 1, T=9) == EP_ERR_INVALID_ARG
+
+
 def test_layout_path_rejects_bad_arguments(eplib):
     AUTO, MULTI, SINGLE = 0, 1, 2
     assert _layout_path_call(eplib, 3) == EP_ERR_INVALID_ARG     # unknown path

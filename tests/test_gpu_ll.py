@@ -1,7 +1,8 @@
 """GPU parity of the low-latency (expert-major) path against the CPU oracle:
-ep_ll_get_dispatch_layout (bit-exact), ep_ll_dispatch (bit-exact bf16 rows,
-E4M3 codes and scales) and ep_ll_combine (the combine tolerance; exact for
-the identity round trip)."""
+ep_ll_get_dispatch_layout (bit-exact, on both kernel paths: multi-launch and
+one thread-block cluster), ep_ll_dispatch (bit-exact bf16 rows, E4M3 codes
+and scales) and ep_ll_combine (the combine tolerance; exact for the identity
+round trip)."""
 from __future__ import annotations
 
 import numpy as np
@@ -32,36 +33,101 @@ def compare_ll_layout(L, want, check_offsets=True):
         np.testing.assert_array_equal(L.ll_src_offset.cpu().numpy(), want.ll_src_offset)
 
 
+PATHS = ["multi", "single"]
+
+
+def ll_layout_on(ep, idx, E, R, path, cap=None, err=None):
+    """The expert-major layout on the given path with poisoned outputs; None
+    (after checking that the call is refused on the host) when the
+    single-launch form does not take this batch."""
+    T, K = idx.shape
+    L = ep.alloc_ll_layout(T, K, E, R, T if cap is None else cap, idx.device)
+    L.ll_slot.fill_(-7)
+    L.ll_count.fill_(-7)
+    L.ll_src_offset.fill_(-7)
+    if path == "single" and not ep.ll_single_launch_fits(T, K, R, E):
+        with pytest.raises(ep.EPError):
+            ep.ll_get_dispatch_layout(idx, E, R, err=err, out=L, path=path)
+        return None
+    ep.ll_get_dispatch_layout(idx, E, R, err=err, out=L, path=path)
+    return L
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("cfg", ll_cases(), ids=lambda c: c.name)
-def test_ll_layout_small(ep, cfg):
+def test_ll_layout_small(ep, cfg, path):
     c = make_case(cfg, with_hidden=False)
     idx, _, _ = device_inputs(c)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    L = ep.ll_get_dispatch_layout(idx, cfg.num_experts, cfg.num_ranks, err=err)
+    L = ll_layout_on(ep, idx, cfg.num_experts, cfg.num_ranks, path, err=err)
+    if L is None:
+        return
     compare_ll_layout(L, oracle.ll_layout(c.topk_idx, cfg.num_experts, cfg.num_ranks,
                                           cfg.num_tokens))
     assert int(err.item()) == 0
 
 
-def test_ll_layout_duplicates_bad_ids_and_capacity(ep):
+def ll_single_launch_cases():
+    """Shapes aimed at the single-launch form: many warps per source, ragged
+    last warps, one-token sources, 2048-slot warps, E = 1024, K = 32, a tight
+    capacity."""
+    specs = [  # name, R, T_r, E, K, routing, mask
+        ("lls_r3_ragged", 3, 1000, 12, 4, "zipf", 0.05),
+        ("lls_r64_tr1", 64, 1, 128, 8, "uniform", 0.0),
+        ("lls_r1_2048slots", 1, 8192, 16, 16, "zipf", 0.1),
+        ("lls_r8_e1024", 8, 300, 1024, 8, "uniform", 0.0),
+        ("lls_r5_k32", 5, 77, 40, 32, "uniform", 0.3),
+        ("lls_r32_decodeish", 32, 100, 256, 8, "zipf", 0.0),
+    ]
+    return [Config(n, R, Tr, 8, E, K, routing=rt, zipf_s=1.2 if rt == "zipf" else 0.0,
+                   mask_prob=m, seed=970 + i)
+            for i, (n, R, Tr, E, K, rt, m) in enumerate(specs)]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("cfg", ll_single_launch_cases(), ids=lambda c: c.name)
+def test_ll_layout_single_launch_shapes(ep, cfg, path):
+    T, K, R, E = cfg.num_tokens, cfg.num_topk, cfg.num_ranks, cfg.num_experts
+    assert ep.ll_single_launch_fits(T, K, R, E)
+    c = make_case(cfg, with_hidden=False)
+    idx, _, _ = device_inputs(c)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L = ll_layout_on(ep, idx, E, R, path, err=err)
+    compare_ll_layout(L, oracle.ll_layout(c.topk_idx, E, R, T))
+    assert int(err.item()) == 0
+    # a capacity below the largest count drops rows and flags it, identically
+    cnt = oracle.ll_layout(c.topk_idx, E, R, T).ll_count
+    cap = max(1, int(cnt.max()) // 2)
+    err.zero_()
+    L = ll_layout_on(ep, idx, E, R, path, cap=cap, err=err)
+    want = oracle.ll_layout(c.topk_idx, E, R, cap)
+    compare_ll_layout(L, want)
+    assert int(err.item()) == want.err_bits
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_ll_layout_duplicates_bad_ids_and_capacity(ep, path):
     idx_np = np.array([[2, 2, 0], [1, 2, -1], [2, 0, 2], [-1, -1, -1], [9, 1, -4], [2, 2, 2]],
                       np.int64)
     idx = torch.from_numpy(idx_np).cuda()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    L = ep.ll_get_dispatch_layout(idx, 3, 1, 3, err=err)
+    L = ll_layout_on(ep, idx, 3, 1, path, cap=3, err=err)
     want = oracle.ll_layout(idx_np, 3, 1, 3)
     assert want.err_bits == 3
     compare_ll_layout(L, want)
     assert int(err.item()) & ep.EP_ERRBIT_BAD_EXPERT and int(err.item()) & ep.EP_ERRBIT_CAPACITY
 
 
+@pytest.mark.parametrize("path", ["auto"] + PATHS)
 @pytest.mark.parametrize("name", ["decode_fp8", "skewed"])
-def test_ll_layout_full_size(ep, name):
+def test_ll_layout_full_size(ep, name, path):
     cfg = CONFIGS[name]
     c, _ = full_case(name)
     idx = torch.from_numpy(c.topk_idx).cuda()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    L = ep.ll_get_dispatch_layout(idx, cfg.num_experts, cfg.num_ranks, err=err)
+    L = ll_layout_on(ep, idx, cfg.num_experts, cfg.num_ranks, path, err=err)
+    if L is None:
+        return
     compare_ll_layout(L, oracle.ll_layout(c.topk_idx, cfg.num_experts, cfg.num_ranks,
                                           cfg.num_tokens))
     assert int(err.item()) == 0

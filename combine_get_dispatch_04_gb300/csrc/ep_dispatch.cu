@@ -10,13 +10,14 @@
 // One warp per token, or per slice of a token when the batch is too small
 // to fill the GPU (slices of a multiple of 32 vectors).  Lanes hold 16-byte
 // vectors of the row (8 bf16 channels); kUnroll vectors per lane are loaded
-// before the stores so each warp keeps 4 x 512 bytes of reads in flight.  Loads bypass L1, stores use
-// the streaming policy.  In the FP8 variant a half-warp holds one block of
-// 128 channels: its amax is taken on the raw bf16 bits (per-halfword unsigned
-// max of |x|, then a 4-step xor-shuffle), one lane per block computes the
+// before the stores so each warp keeps 4 x 512 bytes of reads in flight.
+// Loads bypass L1, stores use the streaming policy.  In the FP8 variant each
+// lane holds two adjacent vectors and 8 lanes hold one block of 128
+// channels: its amax is taken on the raw bf16 bits (per-halfword unsigned
+// max of |x|, then a 3-step xor-shuffle), one lane per block computes the
 // block's two divisions (a warp's 8 blocks in one instruction sequence), and
-// the block is quantised in registers before being written to every
-// destination.  The
+// the block is quantised in registers and written to every destination in
+// 16-byte stores, with the 8 scales of a round in one 32-byte run.  The
 // quantiser rounds exactly as the format definition requires: 448/a and a/448
 // are single correctly rounded divisions (__fdiv_rn), x * (448/a) is a single
 // multiply (__fmul_rn), and the E4M3 conversion is the hardware's
@@ -146,65 +147,72 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_kernel(Args a) {
       }
     }
   } else {
-    // H % 128 == 0 and vbeg % 32 == 0, so vend % 16 == 0: half-warps (one
-    // 128-channel block each) are wholly in or out
+    // Each lane holds two adjacent vectors (16 channels), so a 128-channel
+    // block is 8 lanes and its 16 E4M3 codes per lane go out in one 16-byte
+    // store.  H % 128 == 0 and vbeg % 32 == 0 make vend % 16 == 0, so blocks
+    // are wholly in or out of the slice.
     uint8_t* out = reinterpret_cast<uint8_t*>(a.recv_x);
     const int nblk = a.H / 128;
+    constexpr int kPairs = kUnroll / 2;  // vector pairs per lane and round
     for (int v0 = vbeg; v0 < vend; v0 += 32 * kUnroll) {
       int4 raw[kUnroll];
-      uint32_t mbits[kUnroll];  // amax of the lane's block, as bf16 bits
+      uint32_t mbits[kPairs];  // amax of the lane's block, as bf16 bits
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int v = v0 + u * 32 + lane;
-        raw[u] = v < vend ? ld_stream_v4(src + v) : make_int4(0, 0, 0, 0);
+      for (int u = 0; u < kPairs; ++u) {
+        const int v = v0 + u * 64 + 2 * lane;
+        const bool in = v < vend;
+        raw[2 * u] = in ? ld_stream_v4(src + v) : make_int4(0, 0, 0, 0);
+        raw[2 * u + 1] = in ? ld_stream_v4(src + v + 1) : make_int4(0, 0, 0, 0);
         // for finite bf16 the order of |x| is the unsigned order of the low
         // 15 bits, so a per-halfword unsigned max gives the exact amax bits
-        uint32_t m = __vmaxu2(__vmaxu2((uint32_t)raw[u].x & 0x7FFF7FFFu, (uint32_t)raw[u].y & 0x7FFF7FFFu),
-                              __vmaxu2((uint32_t)raw[u].z & 0x7FFF7FFFu, (uint32_t)raw[u].w & 0x7FFF7FFFu));
+        const int4& p = raw[2 * u];
+        const int4& q = raw[2 * u + 1];
+        uint32_t m = __vmaxu2(
+            __vmaxu2(__vmaxu2((uint32_t)p.x & 0x7FFF7FFFu, (uint32_t)p.y & 0x7FFF7FFFu),
+                     __vmaxu2((uint32_t)p.z & 0x7FFF7FFFu, (uint32_t)p.w & 0x7FFF7FFFu)),
+            __vmaxu2(__vmaxu2((uint32_t)q.x & 0x7FFF7FFFu, (uint32_t)q.y & 0x7FFF7FFFu),
+                     __vmaxu2((uint32_t)q.z & 0x7FFF7FFFu, (uint32_t)q.w & 0x7FFF7FFFu)));
         m = max(m & 0xFFFFu, m >> 16);
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        for (int o = 4; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
         mbits[u] = m;
       }
-      // one correctly rounded division pair for the warp's 2*kUnroll blocks:
-      // lane 2u+h takes block (u, half-warp h), then hands the results back
-      uint32_t mine = 0;
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const uint32_t lo = __shfl_sync(0xFFFFFFFFu, mbits[u], 0);
-        const uint32_t hi = __shfl_sync(0xFFFFFFFFu, mbits[u], 16);
-        if (lane == 2 * u) mine = lo;
-        if (lane == 2 * u + 1) mine = hi;
-      }
+      // one correctly rounded division pair for the round's 8 blocks: lane
+      // i < 8 takes block i (pair u = i / 4, lane group i % 4), in row order
+      const uint32_t m0 = __shfl_sync(0xFFFFFFFFu, mbits[0], 8 * (lane & 3));
+      const uint32_t m1 = __shfl_sync(0xFFFFFFFFu, mbits[1], 8 * (lane & 3));
+      const uint32_t mine = (lane & 4) ? m1 : m0;
       const float am = fmaxf(__uint_as_float(mine << 16), 1e-4f);
       const float sc = __fdiv_rn(am, 448.0f);
       const float iv = __fdiv_rn(448.0f, am);
-      uint2 q[kUnroll];
-      float scale[kUnroll];
+      uint4 qv[kPairs];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int owner = 2 * u + (lane >> 4);
-        const float inv = __shfl_sync(0xFFFFFFFFu, iv, owner);
-        scale[u] = __shfl_sync(0xFFFFFFFFu, sc, owner);
+      for (int u = 0; u < kPairs; ++u) {
+        const float inv = __shfl_sync(0xFFFFFFFFu, iv, 4 * u + (lane >> 3));
         float f[8];
-        unpack_bf16x8(raw[u], f);
-        q[u].x = cvt_e4m3x4(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
-                            __fmul_rn(f[3], inv));
-        q[u].y = cvt_e4m3x4(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv), __fmul_rn(f[6], inv),
-                            __fmul_rn(f[7], inv));
+        unpack_bf16x8(raw[2 * u], f);
+        qv[u].x = cvt_e4m3x4(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
+                             __fmul_rn(f[3], inv));
+        qv[u].y = cvt_e4m3x4(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv), __fmul_rn(f[6], inv),
+                             __fmul_rn(f[7], inv));
+        unpack_bf16x8(raw[2 * u + 1], f);
+        qv[u].z = cvt_e4m3x4(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
+                             __fmul_rn(f[3], inv));
+        qv[u].w = cvt_e4m3x4(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv), __fmul_rn(f[6], inv),
+                             __fmul_rn(f[7], inv));
       }
+      // lanes 0..7 hold the round's 8 scales in row order
+      const bool scale_lane = lane < 8 && v0 + 16 * lane < vend;
       for (int d = 0; d < nd; ++d) {
         const int64_t row = dst_row[warp][d];
         uint8_t* dst = out + row * a.H;
-        float* srow = a.recv_scales + row * nblk;
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int v = v0 + u * 32 + lane;
-          if (v < vend) {
-            st_stream_v2(reinterpret_cast<uint2*>(dst + (int64_t)v * 8), q[u]);
-            if ((lane & 15) == 0) srow[v >> 4] = scale[u];
-          }
+        for (int u = 0; u < kPairs; ++u) {
+          const int v = v0 + u * 64 + 2 * lane;
+          if (v < vend) st_stream_v4(reinterpret_cast<int4*>(dst + (int64_t)v * 8),
+                                     *reinterpret_cast<const int4*>(&qv[u]));
         }
+        if (scale_lane) a.recv_scales[row * nblk + (v0 >> 4) + lane] = sc;
       }
     }
   }

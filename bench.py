@@ -435,7 +435,7 @@ def run_ours(args, cfg: Config):
     # dispatch + combine of that chunk's tokens (compute stream) -> out back
     # (second copy stream).  Every step moves all inputs in and the whole
     # result out.
-    n_chunks = max(1, min(args.e2e_chunks, T // 8192))  # chunks of at least 8192 tokens
+    n_chunks = max(1, min(args.e2e_chunks, T // args.e2e_min_chunk_tokens))
     bounds = [T * i // n_chunks for i in range(n_chunks + 1)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(n_chunks)]      # x chunk landed
@@ -577,6 +577,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="token chunks the end-to-end step pipelines its copies over")
+    ap.add_argument("--e2e-min-chunk-tokens", type=int, default=2048,
+                    help="fewest tokens in one end-to-end chunk (smaller chunks add more host "
+                         "work per step than they overlap)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -420,7 +420,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
   const int t0 = c * tc;
   const int t1 = min(T, t0 + tc);  // t0 < t1: the shape leaves no CTA empty
 
-  for (int i = tid; i < R * E + R * R; i += kCThreads) smem[i] = 0;
+  // only the rows of the sources this CTA holds are ever touched or read
+  const int s_lo = t0 / Tr, s_hi = (t1 - 1) / Tr;
+  for (int i = tid; i < (s_hi - s_lo + 1) * E; i += kCThreads) hist[s_lo * E + i] = 0;
+  for (int i = tid; i < (s_hi - s_lo + 1) * R; i += kCThreads) cnt_sr[s_lo * R + i] = 0;
   __syncthreads();
 
   // --- masks, is_token_in_rank, this CTA's counts and its warps' ballots ---
@@ -469,13 +472,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
   }
   if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && err) atomicOr(err, EP_ERRBIT_BAD_EXPERT);
   __syncthreads();
-  {
-    const int s_lo = t0 / Tr, s_hi = (t1 - 1) / Tr;
-    for (int r = tid; r < R; r += kCThreads) {
-      int v = 0;
-      for (int s = s_lo; s <= s_hi; ++s) v += cnt_sr[s * R + r];
-      tot[r] = v;
-    }
+  for (int r = tid; r < R; r += kCThreads) {
+    int v = 0;
+    for (int s = s_lo; s <= s_hi; ++s) v += cnt_sr[s * R + r];
+    tot[r] = v;
   }
   cluster_arrive();
   cluster_wait();  // every CTA's counts are final and visible to the cluster

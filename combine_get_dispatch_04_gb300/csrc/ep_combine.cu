@@ -433,6 +433,40 @@ bool make_plan(int H, int K, int R, const DeviceProps& p, Plan* out) {
 // and expert-major combine.
 thread_local int g_stall_unit = -1;  // set by ep_debug_set_combine_stall, used once
 
+// Per device and kernel variant: the dynamic shared-memory limit set so far
+// and the blocks per SM at the last queried size.  Set-up calls run only
+// when the size grows or changes, so that steady-state launches make no
+// host calls besides the launch itself (and can be captured in a graph).
+struct Residency {
+  size_t smem_limit = 0;     // cudaFuncAttributeMaxDynamicSharedMemorySize set so far
+  size_t smem_queried = 0;   // size the occupancy below was computed for
+  int resident = 0;
+};
+constexpr int kResidencyDevices = 64;
+std::mutex g_residency_mu;
+Residency g_residency[kResidencyDevices][4];
+
+cudaError_t kernel_residency(void (*kernel)(Args), int which, size_t smem, int* resident) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kResidencyDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_residency_mu);
+  Residency& r = g_residency[dev][which];
+  if (smem > r.smem_limit) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    r.smem_limit = smem;
+  }
+  if (smem != r.smem_queried || r.resident == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r.resident, kernel, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    r.smem_queried = smem;
+  }
+  *resident = r.resident;
+  return cudaSuccess;
+}
+
 ep_status_t launch_combine(Args& a, const DeviceProps& props, ep_stream_t stream) {
   a.stall_unit = g_stall_unit;
   g_stall_unit = -1;
@@ -444,17 +478,13 @@ ep_status_t launch_combine(Args& a, const DeviceProps& props, ep_stream_t stream
   a.nchunk = (a.H + a.C - 1) / a.C;
   // unrolled reductions for up to 8 rows per token (every workload here),
   // with more passes in flight when there are fewer rows
-  void (*kernel)(Args) = a.dmax <= 2   ? combine_kernel<2, 4>
-                         : a.dmax <= 4 ? combine_kernel<4, 2>
-                         : a.dmax <= 8 ? combine_kernel<8, 1>
-                                       : combine_kernel<0, 1>;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)plan.smem) != cudaSuccess)
-    return EP_ERR_CUDA;
+  const int which = a.dmax <= 2 ? 0 : a.dmax <= 4 ? 1 : a.dmax <= 8 ? 2 : 3;
+  void (*kernel)(Args) = which == 0   ? combine_kernel<2, 4>
+                         : which == 1 ? combine_kernel<4, 2>
+                         : which == 2 ? combine_kernel<8, 1>
+                                      : combine_kernel<0, 1>;
   int resident = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, kThreads, plan.smem) !=
-      cudaSuccess)
-    return EP_ERR_CUDA;
+  if (kernel_residency(kernel, which, plan.smem, &resident) != cudaSuccess) return EP_ERR_CUDA;
   if (resident < 1) return EP_ERR_CUDA;
   const int64_t ctas =
       (int64_t)props.sm_count * (resident < plan.ctas_per_sm ? resident : plan.ctas_per_sm);

@@ -529,7 +529,8 @@ def run_ours(args, cfg: Config):
         dom = "dispatch" if dis_ms >= com_ms else "combine"
         kname = {"dispatch": "dispatch_kernel", "combine": "combine_kernel"}[dom]
         src = {"dispatch": "ep_dispatch.cu", "combine": "ep_combine.cu"}[dom]
-        traffic = load_traffic(kname, cfg.name)
+        # expert-major runs have their own captures ("<workload>/ll")
+        traffic = load_traffic(kname, cfg.name + ("/ll" if args.layout == "ll" else ""))
         cpu = None if (args.no_cpu_baseline or world > 1 or args.layout == "ll") else cpu_baseline(case)
         line = {
             "metric": METRIC, "value": whole_job_tokens_per_s(T, world, ms), "unit": UNIT,

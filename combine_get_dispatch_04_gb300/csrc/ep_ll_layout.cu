@@ -8,10 +8,10 @@
 //   ll_slot[t][k] = e*cap + (slots naming e from earlier sources)
 //                   + (slots of src(t) before (t, k) naming e).
 // With the R ranks' tokens laid out rank after rank, that is the global order
-// of slots, so one prefix over 128-token chunks gives every offset.
+// of slots, so one prefix over chunks of 16..128 tokens gives every offset.
 //
 // Three launches, no global atomics:
-//   1. rank   -- one warp per 128-token chunk (chunks never straddle two
+//   1. rank   -- one warp per chunk of 16..128 tokens (chunks never straddle two
 //                source ranks) walks its slots in (token, k) order, 32 at a
 //                time; __match_any_sync ranks equal experts within each step
 //                and a per-expert counter in shared memory carries the rank
@@ -26,11 +26,17 @@
 namespace ep {
 namespace {
 
-constexpr int kChunk = 128;  // tokens per ranking warp
+// Tokens per ranking warp: 128, halved (down to 16) while the batch would
+// give fewer than kMinChunks warps, so that small batches still spread over
+// the GPU.  Depends on (T, R) only, so the workspace size does too.
+constexpr int kMaxChunk = 128;
+constexpr int kMinChunk = 16;
+constexpr int kMinChunks = 1024;
 
 struct LLGeom {
   int64_t T, Tr;
   int K, E, R;
+  int chunk;    // tokens per chunk
   int ncps;     // chunks per source rank
   int nchunks;  // R * ncps
   int64_t cap;  // rows per expert
@@ -43,7 +49,10 @@ LLGeom make_ll_geom(int64_t T, int K, int E, int R, int64_t cap) {
   g.K = K;
   g.E = E;
   g.R = R;
-  g.ncps = (int)((g.Tr + kChunk - 1) / kChunk);
+  g.chunk = kMaxChunk;
+  while (g.chunk > kMinChunk && (int64_t)R * ((g.Tr + g.chunk - 1) / g.chunk) < kMinChunks)
+    g.chunk /= 2;
+  g.ncps = (int)((g.Tr + g.chunk - 1) / g.chunk);
   g.nchunks = R * g.ncps;
   g.cap = cap;
   return g;
@@ -59,8 +68,8 @@ __global__ void __launch_bounds__(32)
   const int lane = threadIdx.x;
   const int ch = blockIdx.x;
   const int s = ch / g.ncps, c = ch % g.ncps;
-  const int64_t t0 = (int64_t)s * g.Tr + (int64_t)c * kChunk;
-  const int64_t len = min((int64_t)kChunk, g.Tr - (int64_t)c * kChunk);
+  const int64_t t0 = (int64_t)s * g.Tr + (int64_t)c * g.chunk;
+  const int64_t len = min((int64_t)g.chunk, g.Tr - (int64_t)c * g.chunk);
   const int64_t nslots = len * g.K;
   const unsigned lt = (1u << lane) - 1u;
   for (int e = lane; e < g.E; e += 32) cnt[e] = 0;
@@ -139,7 +148,7 @@ __global__ void __launch_bounds__(256)
     if (rank >= 0) {
       const int64_t t = i / g.K;
       const int64_t s = t / g.Tr;
-      const int ch = (int)(s * g.ncps + (t - s * g.Tr) / kChunk);
+      const int ch = (int)(s * g.ncps + (t - s * g.Tr) / g.chunk);
       const int e = (int)topk_idx[i];
       const int64_t pos = (int64_t)chunk_off[(int64_t)ch * g.E + e] + rank;
       if (pos < g.cap) {

@@ -300,7 +300,7 @@ ep_status_t ep_ll_get_dispatch_layout(const int64_t* topk_idx, int64_t num_token
  * The expert-major layout's kernels, as for the rank-major layout
  * (ep_layout_path_t):
  *   EP_LAYOUT_MULTI_LAUNCH: three launches over the whole GPU (ranks within
- *     128-token chunks, a prefix over chunks per expert, rows), with
+ *     chunks of 16..128 tokens, a prefix over chunks per expert, rows), with
  *     scratch in the caller's workspace.  Any size.
  *   EP_LAYOUT_SINGLE_LAUNCH: one launch of one thread-block cluster of up to
  *     16 CTAs that exchange per-expert counts through distributed shared

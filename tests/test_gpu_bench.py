@@ -1,0 +1,47 @@
+"""bench.py's GPU arm end to end on the small workload: one JSON line with
+every key of the contract (roofline, cpu_baseline, e2e with its copied
+bytes, the launch count, clocks), and an end-to-end step through host
+buffers that reproduces the device-resident step bit for bit."""
+from __future__ import annotations
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("layout", ["ht", "ll"])
+def test_bench_line_on_the_small_workload(ep, layout):
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--config", "tiny", "--steps", "5",
+           "--warmup", "3", "--layout", layout]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "e2e", "gpu_launches", "clocks"):
+        assert key in d, key
+    assert d["n_gpus"] == 1 and d["steps"] == 5 and d["warmup"] == 3
+    assert d["value"] > 0 and d["config"]["workload"] == "tiny"
+    rf = d["roofline"]
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
+    assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"])
+    e2e = d["e2e"]
+    T, H, K = 512, 256, 4
+    assert e2e["h2d_bytes_per_step"] == T * K * 8 + T * K * 4 + T * H * 2
+    assert e2e["d2h_bytes_per_step"] == T * H * 2
+    assert e2e["check"] == "out matches the device-resident step"
+    # one single-launch layout, dispatch and combine per step
+    assert d["gpu_launches"] == 3 * d["steps"]
+    assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    if layout == "ht":
+        cb = d["cpu_baseline"]
+        assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1

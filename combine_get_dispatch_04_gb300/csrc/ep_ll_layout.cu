@@ -17,8 +17,8 @@
 //                and a per-expert counter in shared memory carries the rank
 //                across steps.  It writes each slot's rank within the chunk
 //                and the chunk's per-expert histogram.
-//   2. scan   -- one warp per expert: exclusive prefix over chunks, the
-//                per-source offsets and the per-expert count.
+//   2. scan   -- one warp per expert: exclusive prefix over chunks (32 per
+//                step, coalesced), the per-source offsets and the count.
 //   3. assign -- one thread per slot: e*cap + chunk offset + rank, with the
 //                capacity check.
 #include "ep_common.cuh"
@@ -104,11 +104,14 @@ __global__ void __launch_bounds__(32)
     }
   }
   if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && err) atomicOr(err, EP_ERRBIT_BAD_EXPERT);
-  for (int e = lane; e < g.E; e += 32) chunk_hist[(int64_t)ch * g.E + e] = cnt[e];
+  // expert-major [E][nchunks], so that the scan reads each expert's chunks
+  // with coalesced loads
+  for (int e = lane; e < g.E; e += 32) chunk_hist[(int64_t)e * g.nchunks + ch] = cnt[e];
 }
 
-// One warp per expert: lanes own contiguous runs of chunks, a warp prefix
-// over the runs, then each lane writes its chunks' offsets.
+// One warp per expert: its chunks 32 at a time (one coalesced load per
+// lane, the next group loaded ahead), a warp scan per group and a running
+// total carried across groups.
 __global__ void __launch_bounds__(256)
     ll_scan_kernel(LLGeom g, const int32_t* __restrict__ chunk_hist, int32_t* __restrict__ chunk_off,
                    int32_t* __restrict__ ll_count, int32_t* __restrict__ ll_src_offset) {
@@ -116,24 +119,27 @@ __global__ void __launch_bounds__(256)
   const int lane = threadIdx.x & 31;
   const int e = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (e >= g.E) return;  // uniform per warp
-  const int seg = (g.nchunks + 31) / 32;
-  const int lo = min(g.nchunks, lane * seg), hi = min(g.nchunks, lo + seg);
-  int sum = 0;
-#pragma unroll 4
-  for (int ch = lo; ch < hi; ++ch) sum += chunk_hist[(int64_t)ch * g.E + e];
-  int incl = sum;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += v;
+  const int32_t* h = chunk_hist + (int64_t)e * g.nchunks;
+  int32_t* off = chunk_off + (int64_t)e * g.nchunks;
+  int run = 0;
+  int v = lane < g.nchunks ? h[lane] : 0;
+  for (int c0 = 0; c0 < g.nchunks; c0 += 32) {
+    const int ch = c0 + lane;
+    const int nxt = ch + 32 < g.nchunks ? h[ch + 32] : 0;
+    int incl = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    const int excl = run + incl - v;
+    if (ch < g.nchunks) {
+      off[ch] = excl;
+      if (ll_src_offset && ch % g.ncps == 0) ll_src_offset[(int64_t)e * g.R + ch / g.ncps] = excl;
+    }
+    run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    v = nxt;
   }
-  int run = incl - sum;
-  for (int ch = lo; ch < hi; ++ch) {
-    const int v = chunk_hist[(int64_t)ch * g.E + e];
-    if (ch % g.ncps == 0 && ll_src_offset) ll_src_offset[(int64_t)e * g.R + ch / g.ncps] = run;
-    chunk_off[(int64_t)ch * g.E + e] = run;
-    run += v;
-  }
-  if (lane == 31 && ll_count) ll_count[e] = incl;
+  if (lane == 0 && ll_count) ll_count[e] = run;
 }
 
 __global__ void __launch_bounds__(256)
@@ -150,7 +156,7 @@ __global__ void __launch_bounds__(256)
       const int64_t s = t / g.Tr;
       const int ch = (int)(s * g.ncps + (t - s * g.Tr) / g.chunk);
       const int e = (int)topk_idx[i];
-      const int64_t pos = (int64_t)chunk_off[(int64_t)ch * g.E + e] + rank;
+      const int64_t pos = (int64_t)chunk_off[(int64_t)e * g.nchunks + ch] + rank;
       if (pos < g.cap) {
         ll_slot[i] = (int32_t)(e * g.cap + pos);
       } else {

@@ -568,6 +568,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(CONFIGS))
+    ap.add_argument("--seed", type=int, default=None,
+                    help="draw the workload with this seed instead of its own")
     ap.add_argument("--tokens-per-rank", type=int, default=None,
                     help="scale the workload (same recipe) for profiling runs")
     ap.add_argument("--layout", choices=["ht", "ll"], default="ht",
@@ -587,6 +589,9 @@ def main(argv=None):
     cfg = CONFIGS[args.config]
     if args.tokens_per_rank:
         cfg = cfg.scaled(args.tokens_per_rank)
+    if args.seed is not None:
+        from dataclasses import replace
+        cfg = replace(cfg, seed=args.seed)
     if args.impl == "reference":
         run_reference(args, cfg)
     else:

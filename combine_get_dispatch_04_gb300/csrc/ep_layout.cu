@@ -9,16 +9,21 @@
 // a token's row in destination r is
 //     slot[t][r] = recv_base[r] + #{t' < t : token t' is sent to r}.
 //
-// Three launches, no atomics on global counters and no inter-block waits:
+// Two forms with identical outputs.  The multi-launch form has no atomics on
+// global counters and no inter-block waits:
 //   1. count  -- one thread per token: rank mask (a 64-bit set), the
 //                is_token_in_rank row, and per-block partial counts per rank
 //                (warp ballots) and per expert (warp-aggregated shared-memory
 //                histogram).  Blocks never straddle two source ranks.
 //   2. scan   -- one block: per-(source, rank) and per-(source, expert)
 //                totals, recv_base, and the exclusive prefix of every block's
-//                count per destination.
+//                count per destination.  Folded into assign when the per-block
+//                counts are few enough for every block to sum them itself.
 //   3. assign -- one thread per token: ballot-based prefix within the block
 //                plus the block's prefix gives the slot.
+// The single-launch form (small batches, further below) does all of it in
+// one thread-block cluster whose CTAs exchange counts through distributed
+// shared memory.
 #include <mutex>
 
 #include "ep_common.cuh"

@@ -245,9 +245,10 @@ ep_status_t ep_dispatch(const void* x, int hidden, const int64_t* topk_idx,
  *   out[t] = bf16_rne( sum over ranks r with slot[t][r] >= 0 of y[slot[t][r]] ),
  * each destination rank's row once.
  * In (device): y [rows, H] bf16 in dispatch's row layout (expert outputs,
- *   one row per (token, rank) pair); topk_idx [T, K] int64; topk_weights
- *   [T, K] float32 (nullable, see above); slot [T, R] int32 from
- *   ep_get_dispatch_layout.
+ *   one row per (token, rank) pair), with rows >= P = recv_base[R] (every
+ *   row a slot names; the call takes no row count, so this is not checked);
+ *   topk_idx [T, K] int64; topk_weights [T, K] float32 (nullable, see
+ *   above); slot [T, R] int32 from ep_get_dispatch_layout.
  * Out (device): out [T, H] bf16, every element written.
  * err_word (device, nullable): EP_ERRBIT_BAD_EXPERT for ids outside [-1, E)
  *   (skipped), EP_ERRBIT_TIMEOUT if a bounded pipeline wait ran out (the
@@ -345,8 +346,9 @@ ep_status_t ep_ll_dispatch(const void* x, int hidden, int64_t num_tokens, int nu
  * ll_slot[t][k] >= 0 of w[t][k] * float(y[ll_slot[t][k]]) ), accumulated in
  * float32 (each expert's output row read once; with topk_weights == NULL
  * every slot weighs 1).  In (device): y [rows, H] bf16 in the expert-major
- * layout, topk_weights [T, K] f32 (nullable), ll_slot [T, K].  Out (device):
- * out [T, H] bf16, every element written.  Staging as ep_combine.
+ * layout, with rows above every row ll_slot names (E * cap suffices; not
+ * checked), topk_weights [T, K] f32 (nullable), ll_slot [T, K].  Out
+ * (device): out [T, H] bf16, every element written.  Staging as ep_combine.
  */
 ep_status_t ep_ll_combine(const void* y, int hidden, const float* topk_weights,
                           int64_t num_tokens, int num_topk, const int32_t* ll_slot, void* out,

@@ -401,6 +401,9 @@ def ll_combine(y: torch.Tensor, topk_weights: torch.Tensor | None, layout: LLLay
     _need(y, "y", torch.bfloat16)
     H = y.shape[1]
     T, K = layout.ll_slot.shape
+    if y.shape[0] < layout.num_rows:
+        raise EPError(f"y must have the layout's {layout.num_rows} rows (E * capacity), "
+                      f"got {y.shape[0]}")
     if topk_weights is not None:
         _need(topk_weights, "topk_weights", torch.float32, (T, K))
     if out is None:

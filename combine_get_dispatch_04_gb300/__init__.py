@@ -102,6 +102,37 @@ def lib() -> C.CDLL:
     return load()
 
 
+# Debug mode (environment EP_DEBUG=1, or set_debug(True)): every call waits
+# for its stream and raises at once if the device error word it was given is
+# non-zero or the kernels failed, naming the call.  Off by default: calls are
+# asynchronous.
+_debug = os.environ.get("EP_DEBUG", "0") not in ("", "0")
+
+_ERRBITS = ((EP_ERRBIT_BAD_EXPERT, "an expert id outside [-1, E)"),
+            (EP_ERRBIT_CAPACITY, "a row at or beyond the receive capacity"),
+            (EP_ERRBIT_TIMEOUT, "a bounded pipeline wait ran out"))
+
+
+def set_debug(on: bool) -> None:
+    """Synchronise and check the error word after every call (see above)."""
+    global _debug
+    _debug = bool(on)
+
+
+def describe_error_word(value: int) -> str:
+    names = [text for bit, text in _ERRBITS if value & bit]
+    return ", ".join(names) if names else "no error"
+
+
+def _debug_check(what: str, err: torch.Tensor | None, device: torch.device):
+    if not _debug:
+        return
+    torch.cuda.current_stream(device).synchronize()  # raises on a kernel fault
+    if err is not None and int(err.item()) != 0:
+        v = int(err.item())
+        raise EPError(f"{what}: device error word {v} ({describe_error_word(v)})")
+
+
 def _check(status: int, what: str):
     if status != EP_OK:
         msg = lib().ep_status_string(status).decode()
@@ -196,6 +227,7 @@ def get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int
     else:
         _check(lib().ep_get_dispatch_layout_path(*args, LAYOUT_PATHS[path], stream),
                "ep_get_dispatch_layout_path")
+    _debug_check("get_dispatch_layout", err, topk_idx.device)
     return L
 
 
@@ -264,6 +296,7 @@ def dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor
         _ptr(out.recv_scales), _ptr(out.recv_src_idx), _ptr(out.recv_topk_idx),
         _ptr(out.recv_topk_weights), _ptr(out.num_recv_tokens_per_expert), _ptr(err),
         _stream(x.device)), "ep_dispatch")
+    _debug_check("dispatch", err, x.device)
     return out
 
 
@@ -289,6 +322,7 @@ def combine(y: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor 
     _check(lib().ep_combine(_ptr(y), H, _ptr(topk_idx), _ptr(topk_weights), T, K, E, R,
                             _ptr(layout.slot), _ptr(out), _ptr(err), _stream(y.device)),
            "ep_combine")
+    _debug_check("combine", err, y.device)
     return out
 
 
@@ -363,6 +397,7 @@ def ll_get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: 
     else:
         _check(lib().ep_ll_get_dispatch_layout_path(*args, LAYOUT_PATHS[path], _stream(dev)),
                "ep_ll_get_dispatch_layout_path")
+    _debug_check("ll_get_dispatch_layout", err, dev)
     return L
 
 
@@ -393,6 +428,7 @@ def ll_dispatch(x: torch.Tensor, layout: LLLayout, *, use_fp8: bool = False,
                                 int(use_fp8), _ptr(out.recv_x), _ptr(out.recv_scales),
                                 _ptr(out.recv_src_idx), _ptr(err), _stream(x.device)),
            "ep_ll_dispatch")
+    _debug_check("ll_dispatch", err, x.device)
     return out
 
 
@@ -413,4 +449,5 @@ def ll_combine(y: torch.Tensor, topk_weights: torch.Tensor | None, layout: LLLay
         _need(err, "err", torch.int32)
     _check(lib().ep_ll_combine(_ptr(y), H, _ptr(topk_weights), T, K, _ptr(layout.ll_slot),
                                _ptr(out), _ptr(err), _stream(y.device)), "ep_ll_combine")
+    _debug_check("ll_combine", err, y.device)
     return out

@@ -178,3 +178,11 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
             ep.load(str(tmp_path / "missing.so"))
     finally:
         ep._lib = saved
+
+
+def test_error_word_description():
+    import combine_get_dispatch_04_gb300 as ep
+    assert ep.describe_error_word(0) == "no error"
+    assert "expert id" in ep.describe_error_word(ep.EP_ERRBIT_BAD_EXPERT)
+    both = ep.describe_error_word(ep.EP_ERRBIT_CAPACITY | ep.EP_ERRBIT_TIMEOUT)
+    assert "capacity" in both and "wait" in both

@@ -35,6 +35,11 @@
  *   - Limits: 1 <= R <= EP_MAX_RANKS, 1 <= K <= EP_MAX_TOPK,
  *     1 <= E <= EP_MAX_EXPERTS, H % 8 == 0 (H % 128 == 0 for FP8),
  *     T * R < 2^31.
+ *   - The first call of each kind on a device does a one-time set-up on
+ *     the host (kernel attributes, occupancy and cluster-size queries,
+ *     cached per device; thread-safe).  Later calls make no host calls but
+ *     the launches, so a sequence of calls can be captured into a CUDA
+ *     graph once each kind has run eagerly on that device.
  */
 #ifndef EP_H_
 #define EP_H_

@@ -37,9 +37,9 @@
  *     T * R < 2^31.
  *   - The first call of each kind on a device does a one-time set-up on
  *     the host (kernel attributes, occupancy and cluster-size queries,
- *     cached per device; thread-safe).  Later calls make no host calls but
- *     the launches, so a sequence of calls can be captured into a CUDA
- *     graph once each kind has run eagerly on that device.
+ *     cached per device; thread-safe).  Later calls repeat none of it: they
+ *     check arguments and launch, so a sequence of calls can be captured
+ *     into a CUDA graph once each kind has run eagerly on that device.
  */
 #ifndef EP_H_
 #define EP_H_

@@ -655,16 +655,20 @@ extern "C" ep_status_t ep_get_dispatch_layout_path(
     if (!single && (!workspace || !aligned16(workspace))) return EP_ERR_INVALID_ARG;
   }
   const Geom g = make_geom(num_tokens, num_topk, num_experts, num_ranks);
+  const Workspace ws = carve(g, workspace);
   if (single) {
     if (launch_layout_cluster(topk_idx, g, num_tokens_per_rank, num_tokens_per_expert,
                               is_token_in_rank, slot, recv_base, err_word,
-                              to_cuda(stream)) != cudaSuccess) {
-      cudaGetLastError();  // clear the launch error; the status reports it
+                              to_cuda(stream)) == cudaSuccess)
+      return EP_OK;
+    cudaGetLastError();  // clear the launch error
+    // EP_LAYOUT_AUTO runs the multi-launch form instead when the device
+    // refused the cluster (for instance a partition with too few free SMs)
+    // and the caller passed a usable workspace; otherwise report the error.
+    if (path != EP_LAYOUT_AUTO || !workspace || !aligned16(workspace) ||
+        workspace_bytes < ws.bytes)
       return EP_ERR_CUDA;
-    }
-    return EP_OK;
   }
-  const Workspace ws = carve(g, workspace);
   if (num_tokens > 0 && workspace_bytes < ws.bytes) return EP_ERR_CAPACITY;
   launch_layout(topk_idx, g, ws, num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank,
                 slot, recv_base, err_word, to_cuda(stream));

@@ -418,12 +418,15 @@ extern "C" ep_status_t ep_ll_get_dispatch_layout_path(
   if (num_tokens > 0 && !single && (!workspace || !aligned16(workspace))) return EP_ERR_INVALID_ARG;
   cudaStream_t st = to_cuda(stream);
   if (single) {
-    if (launch_ll_cluster(topk_idx, g, ll_slot, ll_count, ll_src_offset, err_word, st) !=
-        cudaSuccess) {
-      cudaGetLastError();  // clear the launch error; the status reports it
+    if (launch_ll_cluster(topk_idx, g, ll_slot, ll_count, ll_src_offset, err_word, st) ==
+        cudaSuccess)
+      return EP_OK;
+    cudaGetLastError();  // clear the launch error
+    // EP_LAYOUT_AUTO runs the three-launch form instead when the device
+    // refused the cluster and the caller passed a usable workspace.
+    if (path != EP_LAYOUT_AUTO || !workspace || !aligned16(workspace) ||
+        workspace_bytes < ll_ws_bytes(g))
       return EP_ERR_CUDA;
-    }
-    return EP_OK;
   }
   const size_t half = align_up(sizeof(int32_t) * (size_t)g.nchunks * g.E, 256);
   if (num_tokens > 0 && workspace_bytes < ll_ws_bytes(g)) return EP_ERR_CAPACITY;

@@ -131,6 +131,9 @@ ep_status_t ep_get_dispatch_layout(const int64_t* topk_idx, int64_t num_tokens, 
  *   Internode HT); this fused form has no counterpart there.
  * EP_LAYOUT_AUTO: the single-launch form where it is the faster one
  *   (ep_layout_auto_single_launch: it fits and T <= 8192), else multi-launch.
+ *   Should the device refuse the cluster launch (a partition with too few
+ *   free SMs, say), AUTO runs the multi-launch form instead if a usable
+ *   workspace was passed, and returns EP_ERR_CUDA if not.
  */
 typedef enum {
   EP_LAYOUT_AUTO = 0,
@@ -316,6 +319,8 @@ ep_status_t ep_ll_get_dispatch_layout(const int64_t* topk_idx, int64_t num_token
  *     when R divides 64).
  *   EP_LAYOUT_AUTO: the single launch whenever it fits (measured faster
  *     at every size it takes); ep_ll_layout_auto_single_launch says which.
+ *     As for the rank-major layout, AUTO falls back to the three launches
+ *     if the device refuses the cluster and a usable workspace was passed.
  * Both give identical outputs.  EP_LAYOUT_SINGLE_LAUNCH on a batch that does
  * not fit (T = 0 included) returns EP_ERR_INVALID_ARG with nothing enqueued.
  */

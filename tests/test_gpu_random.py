@@ -1,10 +1,11 @@
 """Randomised parity sweep (48 cases; EP_RANDOM_CASES=n for more): many
-small seeded shapes (ranks 1..64, ragged tokens per rank, 1..8 experts per rank, top-1..12, hidden sizes from one
-16-byte vector up, uniform or Zipf routing, 0-50% masked slots), each run
-through every entry point and compared with the CPU oracle: both layouts on
-both kernel paths (bit-exact), both dispatches (bit-exact bf16 rows; E4M3
-codes and scales where H % 128 == 0), and the weighted and unweighted
-combines (the combine tolerance)."""
+small seeded shapes (ranks 1..64, ragged tokens per rank, 1..8 experts per
+rank, top-1..12, hidden sizes from one 16-byte vector up, uniform or Zipf
+routing, 0-50% masked slots), each run through every entry point and
+compared with the CPU oracle: both layouts on both kernel paths (bit-exact),
+both dispatches (bit-exact bf16 rows; E4M3 codes and scales where
+H % 128 == 0), and the weighted and unweighted combines (the combine
+tolerance)."""
 from __future__ import annotations
 
 import os

@@ -57,3 +57,40 @@ def test_two_streams_do_not_interfere(ep, path):
             assert torch.equal(LLa.ll_slot, LLb.ll_slot) and torch.equal(LLa.ll_count, LLb.ll_count)
             live = LLa.ll_slot[LLa.ll_slot >= 0].long()
             np.testing.assert_array_equal(bits_of(dla.recv_x[live]), bits_of(dlb.recv_x[live]))
+
+
+def test_two_host_threads_on_their_own_streams(ep):
+    """The library's per-device caches are shared by host threads (and filled
+    under a lock); two threads, each with its own stream and buffers, calling
+    at the same time get the same results as one thread alone."""
+    import threading
+    cfgs = [Config("h0", 4, 500, 256, 32, 4, routing="zipf", zipf_s=1.2, seed=41),
+            Config("h1", 4, 500, 256, 32, 4, mask_prob=0.2, seed=42)]
+    cases = [make_case(c) for c in cfgs]
+    ins = [device_inputs(c) for c in cases]
+    E, R = cfgs[0].num_experts, cfgs[0].num_ranks
+    want = [bits_of(_step(ep, *ins[i], E, R, "auto", False)[2]) for i in (0, 1)]
+    got = [[], []]
+    errors = []
+
+    def worker(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(10):
+                    out = _step(ep, *ins[i], E, R, "auto", False)[2]
+                    s.synchronize()
+                    got[i].append(bits_of(out))
+        except Exception as e:  # reported below, in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in (0, 1)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for i in (0, 1):
+        assert len(got[i]) == 10
+        for g in got[i]:
+            np.testing.assert_array_equal(g, want[i])

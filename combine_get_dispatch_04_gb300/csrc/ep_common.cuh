@@ -244,6 +244,22 @@ __device__ __forceinline__ void bulk_load_g2s(void* dst_smem, const void* src_gl
       : "memory");
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Stores with an L2 cache-policy hint (from createpolicy).
+__device__ __forceinline__ void st_hint_b32(void* p, uint32_t v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void st_hint_b64(void* p, uint64_t v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(p), "l"(v), "l"(policy)
+               : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -115,17 +115,23 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_kernel(Args a) {
     for (int d = lane; d < nd; d += 32) a.recv_src_idx[dst_row[warp][d]] = (int32_t)t;
   }
   if (slice == 0 && a.rank_meta && (a.recv_src_idx || a.recv_topk_idx || a.recv_topk_w)) {
+    // keep the small metadata rows in L2 (evict-last) until neighbouring
+    // rows, written by other warps, have filled their sectors
+    const uint64_t keep = l2_policy_evict_last();
     const int64_t e = lane < a.K ? a.topk_idx[t * a.K + lane] : -1;
     const float w = (lane < a.K && a.topk_w) ? a.topk_w[t * a.K + lane] : 0.0f;
     const int er = (e >= 0 && e < a.E) ? (int)(e / a.El) : -1;
     for (int d = 0; d < nd; ++d) {
       const int64_t row = dst_row[warp][d];
       const int r = dst_rank[warp][d];
-      if (lane == 0 && a.recv_src_idx) a.recv_src_idx[row] = (int32_t)t;
+      if (lane == 0 && a.recv_src_idx) st_hint_b32(a.recv_src_idx + row, (uint32_t)t, keep);
       if (lane < a.K) {
         const bool here = er == r;
-        if (a.recv_topk_idx) a.recv_topk_idx[row * a.K + lane] = here ? e - (int64_t)r * a.El : -1;
-        if (a.recv_topk_w) a.recv_topk_w[row * a.K + lane] = here ? w : 0.0f;
+        if (a.recv_topk_idx)
+          st_hint_b64(a.recv_topk_idx + row * a.K + lane,
+                      (uint64_t)(here ? e - (int64_t)r * a.El : -1), keep);
+        if (a.recv_topk_w)
+          st_hint_b32(a.recv_topk_w + row * a.K + lane, __float_as_uint(here ? w : 0.0f), keep);
       }
     }
   }

@@ -242,7 +242,13 @@ __device__ __forceinline__ void reduce_rows(const uint8_t* stage, int C, int ch0
 
 template <int kDMax, int kP>
 __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
-  pdl_wait_then_release();
+  // The grid is persistent (every block resident from the start), so an
+  // early release would gain no launch overlap; it would only let the next
+  // kernel's blocks take SMs as this grid drains, unevenly.  On one GB300
+  // an early release here cost the following step 54 us on 131072 skewed
+  // tokens (1584 against 1638 us) and 48 us on Mixtral, and saved nothing
+  // on the others.
+  pdl_wait();
   extern __shared__ __align__(128) uint8_t smem[];
   const SmemLayout lay = smem_layout(a.S, a.stage_bytes, a.dmax);
   uint8_t* tiles = smem;

@@ -154,6 +154,11 @@ __device__ __forceinline__ void pdl_wait_then_release() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+// Waits like pdl_wait_then_release but leaves the release to the implicit
+// one at block exit: the next kernel is scheduled only once every block of
+// this grid has finished.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // bounded pipeline waits: 1 s
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

@@ -1,7 +1,8 @@
 """bench.py's GPU arm end to end on the small workload: one JSON line with
 every key of the contract (roofline, cpu_baseline, e2e with its copied
 bytes, the launch count, clocks), and an end-to-end step through host
-buffers that reproduces the device-resident step bit for bit."""
+buffers that reproduces the device-resident step bit for bit, also with the
+plain steps timed as CUDA-graph replays."""
 from __future__ import annotations
 
 import json
@@ -16,10 +17,10 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("layout", ["ht", "ll"])
-def test_bench_line_on_the_small_workload(ep, layout):
+@pytest.mark.parametrize("layout,graph", [("ht", False), ("ll", False), ("ht", True)])
+def test_bench_line_on_the_small_workload(ep, layout, graph):
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--config", "tiny", "--steps", "5",
-           "--warmup", "3", "--layout", layout]
+           "--warmup", "3", "--layout", layout] + (["--graph"] if graph else [])
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-3000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
@@ -42,6 +43,12 @@ def test_bench_line_on_the_small_workload(ep, layout):
     # one single-launch layout, dispatch and combine per step
     assert d["gpu_launches"] == 3 * d["steps"]
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    # the per-kernel times come from a second pass of the same number of steps
+    kt = d["kernel_timing"]
+    assert kt["steps"] == 5 and kt["ms_per_step"] > 0
+    parts = sum(d["kernels"][k]["ms"] for k in ("layout", "dispatch", "combine"))
+    assert parts == pytest.approx(kt["ms_per_step"], rel=0.02)
+    assert (d["config"].get("step_launch") == "cuda_graph_replay") == graph
     if layout == "ht":
         cb = d["cpu_baseline"]
         assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1

@@ -42,7 +42,10 @@ EXPORTED = ("ep_status_string", "ep_workspace_bytes", "ep_get_dispatch_layout",
             "ep_combine", "ep_ll_workspace_bytes", "ep_ll_get_dispatch_layout",
             "ep_ll_dispatch", "ep_ll_combine", "ep_debug_set_combine_stall",
             "ep_ll_layout_single_launch_fits", "ep_ll_layout_auto_single_launch",
-            "ep_ll_get_dispatch_layout_path")
+            "ep_ll_get_dispatch_layout_path", "ep_combine_sched", "ep_ll_combine_sched")
+
+# 64-bit words of a combine's scheduling counters (EP_COMBINE_SCHED_WORDS)
+COMBINE_SCHED_WORDS = 2
 
 _lib = None
 
@@ -89,10 +92,12 @@ def load(path: str | None = None) -> C.CDLL:
         getattr(L, name).restype = i32
     L.ep_ll_dispatch.argtypes = [P, i32, i64, i32, P, i64, i32, P, P, P, P, P]
     L.ep_ll_combine.argtypes = [P, i32, P, i64, i32, P, P, P, P]
+    L.ep_combine_sched.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, P, P, P]
+    L.ep_ll_combine_sched.argtypes = [P, i32, P, i64, i32, P, P, P, P, P]
     for name in ("ep_get_dispatch_layout", "ep_get_dispatch_layout_path",
                  "ep_layout_total_rows", "ep_dispatch", "ep_combine",
                  "ep_ll_get_dispatch_layout", "ep_ll_get_dispatch_layout_path",
-                 "ep_ll_dispatch", "ep_ll_combine"):
+                 "ep_ll_dispatch", "ep_ll_combine", "ep_combine_sched", "ep_ll_combine_sched"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -169,6 +174,10 @@ class Layout:
     num_experts: int
     num_ranks: int
     workspace: torch.Tensor | None = None
+    # [2] int64 counters of the dynamically scheduled combine, zero between
+    # launches; None: the static schedule.  One Layout's combines run in
+    # order on one stream (or in one graph), never two at once.
+    sched: torch.Tensor | None = None
 
     @property
     def num_tokens(self) -> int:
@@ -189,6 +198,12 @@ def auto_single_launch(num_tokens: int, num_ranks: int, num_experts: int) -> boo
     return bool(lib().ep_layout_auto_single_launch(num_tokens, num_ranks, num_experts))
 
 
+def alloc_combine_sched(device: torch.device) -> torch.Tensor:
+    """Zeroed counters for the dynamically scheduled combine (each launch
+    leaves them zero again)."""
+    return torch.zeros(COMBINE_SCHED_WORDS, dtype=torch.int64, device=device)
+
+
 def alloc_layout(num_tokens: int, num_experts: int, num_ranks: int,
                  device: torch.device) -> Layout:
     """Output tensors and the multi-launch workspace (allocated for every size,
@@ -198,7 +213,8 @@ def alloc_layout(num_tokens: int, num_experts: int, num_ranks: int,
     ws = torch.empty(max(workspace_bytes(T, R, E), 16), dtype=torch.uint8, device=device)
     return Layout(torch.empty((R, R), **i32), torch.empty((R, E), **i32),
                   torch.empty((T, R), dtype=torch.bool, device=device),
-                  torch.empty((T, R), **i32), torch.empty(R + 1, **i32), E, R, ws)
+                  torch.empty((T, R), **i32), torch.empty(R + 1, **i32), E, R, ws,
+                  alloc_combine_sched(device))
 
 
 def get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int, *,
@@ -300,6 +316,15 @@ def dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor
     return out
 
 
+def _sched_of(layout, device: torch.device) -> torch.Tensor | None:
+    s = layout.sched
+    if s is not None:
+        _need(s, "sched", torch.int64, (COMBINE_SCHED_WORDS,))
+        if s.device != device:
+            raise EPError("the layout's sched must be on the combine's device")
+    return s
+
+
 def combine(y: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor | None,
             layout: Layout, *, err: torch.Tensor | None = None,
             out: torch.Tensor | None = None) -> torch.Tensor:
@@ -319,9 +344,10 @@ def combine(y: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor 
     _need(out, "out", torch.bfloat16, (T, H))
     if err is not None:
         _need(err, "err", torch.int32)
-    _check(lib().ep_combine(_ptr(y), H, _ptr(topk_idx), _ptr(topk_weights), T, K, E, R,
-                            _ptr(layout.slot), _ptr(out), _ptr(err), _stream(y.device)),
-           "ep_combine")
+    sched = _sched_of(layout, y.device)
+    _check(lib().ep_combine_sched(_ptr(y), H, _ptr(topk_idx), _ptr(topk_weights), T, K, E, R,
+                                  _ptr(layout.slot), _ptr(out), _ptr(sched), _ptr(err),
+                                  _stream(y.device)), "ep_combine_sched")
     _debug_check("combine", err, y.device)
     return out
 
@@ -339,6 +365,7 @@ class LLLayout:
     num_ranks: int
     expert_capacity: int
     workspace: torch.Tensor | None = None
+    sched: torch.Tensor | None = None  # as Layout.sched
 
     @property
     def num_rows(self) -> int:
@@ -353,7 +380,8 @@ def alloc_ll_layout(num_tokens: int, num_topk: int, num_experts: int, num_ranks:
     return LLLayout(torch.empty((num_tokens, num_topk), dtype=torch.int32, device=device),
                     torch.empty(num_experts, dtype=torch.int32, device=device),
                     torch.empty((num_experts, num_ranks), dtype=torch.int32, device=device),
-                    num_experts, num_ranks, int(expert_capacity), ws)
+                    num_experts, num_ranks, int(expert_capacity), ws,
+                    alloc_combine_sched(device))
 
 
 def ll_single_launch_fits(num_tokens: int, num_topk: int, num_ranks: int,
@@ -447,7 +475,9 @@ def ll_combine(y: torch.Tensor, topk_weights: torch.Tensor | None, layout: LLLay
     _need(out, "out", torch.bfloat16, (T, H))
     if err is not None:
         _need(err, "err", torch.int32)
-    _check(lib().ep_ll_combine(_ptr(y), H, _ptr(topk_weights), T, K, _ptr(layout.ll_slot),
-                               _ptr(out), _ptr(err), _stream(y.device)), "ep_ll_combine")
+    sched = _sched_of(layout, y.device)
+    _check(lib().ep_ll_combine_sched(_ptr(y), H, _ptr(topk_weights), T, K, _ptr(layout.ll_slot),
+                                     _ptr(out), _ptr(sched), _ptr(err), _stream(y.device)),
+           "ep_ll_combine_sched")
     _debug_check("ll_combine", err, y.device)
     return out

@@ -12,12 +12,19 @@
 //
 // Design: persistent CTAs, several per SM, three warp roles per CTA, all
 // communication through mbarriers in shared memory.
-//   - warp 1 (routing): for batches of 32 tokens, each lane gathers one
-//     token's routing into a double-buffered table: the token's distinct
-//     destination rows (each row is read from HBM once, however many of the
-//     token's slots name that rank) and, per row, the sum of the weights of
-//     the slots naming its rank.  Loads are issued eight at a time, and the
-//     warp runs one batch ahead of the copies.
+//   - Tokens go out in batches of a few (up to 32).  Each CTA's first batch
+//     is fixed; with a scheduling counter (the _sched entry points) every
+//     further batch is claimed from it with one atomic, so CTAs that the
+//     memory system serves faster take more batches and all finish within
+//     about a batch of each other.  Without it CTA b takes every grid-th
+//     batch.  The last CTA to exit returns the counter to zero.
+//   - warp 1 (routing): claims the next batch before it needs it, and for
+//     each batch each lane gathers one token's routing into a
+//     double-buffered table (headed by the batch's first token and size):
+//     the token's distinct destination rows (each row is read from HBM once,
+//     however many of the token's slots name that rank) and, per row, the
+//     sum of the weights of the slots naming its rank.  Loads are issued
+//     eight at a time, and the warp runs one batch ahead of the copies.
 //   - warp 0 (copies): per (token, channel chunk) it waits for a free stage,
 //     posts the byte count on the stage's "full" barrier and issues one 1-D
 //     bulk copy per distinct row (lane j copies row j), with an L2
@@ -39,6 +46,8 @@
 // EP_ERRBIT_TIMEOUT, stops issuing, waits (bounded) for the copies it has in
 // flight, and returns.
 #include <cuda_bf16.h>
+
+#include <cmath>
 
 #include "ep_common.cuh"
 
@@ -69,11 +78,13 @@ struct Args {
   int dmax;    // rows per stage = min(K, R)
   uint32_t stage_bytes;
   int stall_unit;  // test hook: CTA 0 never arms this pipeline unit (-1: off)
+  unsigned long long* sched;  // [2] claimed-batch and exited-block counters (null: static batches)
+  int claim;                  // tokens per batch
 };
 
 // Offsets of the shared-memory regions that follow the S row tiles.
 struct SmemLayout {
-  size_t bars, rows, w, D, abort, total;
+  size_t bars, rows, w, D, hdr, abort, total;
 };
 
 __host__ __device__ inline size_t al(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -89,6 +100,9 @@ __host__ __device__ inline SmemLayout smem_layout(int S, uint32_t stage_bytes, i
   off += sizeof(float) * 2 * kBatch * (size_t)dmax;
   L.D = off;
   off += sizeof(int32_t) * 2 * kBatch;
+  off = al(off, 8);
+  L.hdr = off;
+  off += sizeof(int64_t) * 2 + sizeof(int32_t) * 2;
   off = al(off, 16);
   L.abort = off;
   off += 16;
@@ -259,6 +273,8 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
   int32_t* trows = reinterpret_cast<int32_t*>(smem + lay.rows);  // [2][kBatch][dmax]
   float* tW = reinterpret_cast<float*>(smem + lay.w);            // [2][kBatch][dmax]
   int32_t* tD = reinterpret_cast<int32_t*>(smem + lay.D);        // [2][kBatch]
+  int64_t* tT0 = reinterpret_cast<int64_t*>(smem + lay.hdr);      // [2] first token of the batch
+  int32_t* tN = reinterpret_cast<int32_t*>(tT0 + 2);              // [2] its tokens (0: no more)
   volatile int* abort = reinterpret_cast<volatile int*>(smem + lay.abort);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
@@ -276,27 +292,38 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
   }
   __syncthreads();
 
-  // this CTA's tokens: a contiguous range, balanced to within one token
-  const int64_t tb = a.T * blockIdx.x / gridDim.x;
-  const int64_t te = a.T * (blockIdx.x + 1) / gridDim.x;
+  // Batches of a.claim tokens: block b's first is [b * claim, (b + 1) * claim).
+  // With a.sched the rest are claimed from a.sched[0] (offset by
+  // gridDim.x * claim), so blocks that are served faster take more of them;
+  // without it block b takes every gridDim.x-th batch after its first.
+  const int64_t claim = a.claim;
+  const int64_t dyn0 = (int64_t)gridDim.x * claim;
 
   if (warp == 1) {
     // ------------------------------------------------------------ routing
     bool ok = true, bad = false;
-    uint32_t bi = 0;
-    for (int64_t t0 = tb; t0 < te; t0 += kBatch, ++bi) {
+    int64_t t0 = (int64_t)blockIdx.x * claim;
+    for (uint32_t bi = 0;; ++bi) {
       const int buf = bi & 1;
       const uint32_t use = bi >> 1;
+      unsigned long long nxt = 0;  // the next batch, claimed before it is needed
+      if (a.sched && t0 < a.T && lane == 0) nxt = atomicAdd(a.sched, (unsigned long long)claim);
       if (use > 0 && !wait_warp(&tempty[buf], (use - 1) & 1, abort)) {
         ok = false;
         break;
       }
-      const int n = (int)(te - t0 < kBatch ? te - t0 : kBatch);
+      const int n = t0 < a.T ? (int)(a.T - t0 < claim ? a.T - t0 : claim) : 0;
+      if (lane == 0) {
+        tT0[buf] = t0;
+        tN[buf] = n;
+      }
       if (lane < n) {
         const size_t e = (size_t)buf * kBatch + lane;
         tD[e] = gather_token(a, t0 + lane, trows + e * a.dmax, tW + e * a.dmax, bad);
       }
       mbar_arrive(&tfull[buf]);  // every lane releases its own table writes
+      if (n == 0) break;
+      t0 = a.sched ? dyn0 + (int64_t)__shfl_sync(0xFFFFFFFFu, nxt, 0) : t0 + dyn0;
     }
     if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && a.err) atomicOr(a.err, EP_ERRBIT_BAD_EXPERT);
     if (!ok && lane == 0) {
@@ -308,13 +335,14 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
     const uint64_t policy = l2_policy_evict_first();
     uint32_t it = 0, bi = 0;
     bool ok = true;
-    for (int64_t t0 = tb; t0 < te && ok; t0 += kBatch, ++bi) {
+    for (; ok; ++bi) {
       const int buf = bi & 1;
       if (!wait_warp(&tfull[buf], (bi >> 1) & 1, abort)) {
         ok = false;
         break;
       }
-      const int n = (int)(te - t0 < kBatch ? te - t0 : kBatch);
+      const int n = tN[buf];
+      if (n == 0) break;
       for (int i = 0; i < n && ok; ++i) {
         const size_t e = (size_t)buf * kBatch + i;
         const int D = tD[e];
@@ -355,9 +383,15 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
     const int ct = threadIdx.x - 64;
     uint32_t it = 0, bi = 0;
     bool ok = true;
-    for (int64_t t0 = tb; t0 < te && ok; t0 += kBatch, ++bi) {
+    for (; ok; ++bi) {
       const int buf = bi & 1;
-      const int n = (int)(te - t0 < kBatch ? te - t0 : kBatch);
+      if (!wait_warp(&tfull[buf], (bi >> 1) & 1, abort)) {
+        ok = false;
+        break;
+      }
+      const int n = tN[buf];
+      const int64_t t0 = tT0[buf];
+      if (n == 0) break;
       for (int i = 0; i < n && ok; ++i) {
         const size_t e = (size_t)buf * kBatch + i;
         const float* Wsm = tW + e * a.dmax;
@@ -392,6 +426,18 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
     if (!ok && lane == 0) {
       *abort = 1;
       if (a.err) atomicOr(a.err, EP_ERRBIT_TIMEOUT);
+    }
+  }
+  // The last block to leave resets the counters for the next launch: every
+  // block has stopped claiming by then.
+  if (!a.sched) return;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.sched + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
+      __threadfence();
+      a.sched[0] = 0;
+      a.sched[1] = 0;
     }
   }
 }
@@ -473,6 +519,22 @@ cudaError_t kernel_residency(void (*kernel)(Args), int which, size_t smem, int* 
   return cudaSuccess;
 }
 
+// Tokens per batch for a grid of `ctas` blocks.  At least T / (64 * ctas),
+// so that every block takes many batches and the faster blocks absorb the
+// slower ones' share.  And at least enough that the claims on the one
+// counter stay under about 100 per microsecond: same-address atomics on
+// GB300 saturated between 130 and 170 per us (batches of one token took
+// skewed routing from 1544 to 1720 us per step).  The rate is estimated
+// from a 6.6 TB/s gather of 1 + min(K, R) rows of H channels per token,
+// over at least 10 us.
+int claim_tokens(int64_t T, int64_t ctas, int H, int dmax) {
+  int64_t c = T / (ctas * 64);
+  const double us = fmax(10.0, (double)T * 2.0 * H * (1 + dmax) / 6.6e6);
+  const int64_t by_rate = (int64_t)ceil((double)T / us / 100.0);
+  if (c < by_rate) c = by_rate;
+  return (int)(c < 1 ? 1 : c > kBatch ? kBatch : c);
+}
+
 ep_status_t launch_combine(Args& a, const DeviceProps& props, ep_stream_t stream) {
   a.stall_unit = g_stall_unit;
   g_stall_unit = -1;
@@ -494,7 +556,9 @@ ep_status_t launch_combine(Args& a, const DeviceProps& props, ep_stream_t stream
   if (resident < 1) return EP_ERR_CUDA;
   const int64_t ctas =
       (int64_t)props.sm_count * (resident < plan.ctas_per_sm ? resident : plan.ctas_per_sm);
-  const int64_t grid = a.T < ctas ? a.T : ctas;
+  a.claim = claim_tokens(a.T, ctas, a.H, a.dmax);
+  const int64_t batches = (a.T + a.claim - 1) / a.claim;
+  const int64_t grid = batches < ctas ? batches : ctas;
   launch_pdl(kernel, (unsigned)grid, kThreads, plan.smem, to_cuda(stream), a);
   return launch_status();
 }
@@ -503,15 +567,21 @@ ep_status_t launch_combine(Args& a, const DeviceProps& props, ep_stream_t stream
 
 using namespace ep;
 
-extern "C" ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk_idx,
-                                  const float* topk_weights, int64_t num_tokens, int num_topk,
-                                  int num_experts, int num_ranks, const int32_t* slot, void* out,
-                                  int32_t* err_word, ep_stream_t stream) {
+namespace {
+
+bool sched_ok(const uint64_t* sched) {
+  return sched == nullptr || (reinterpret_cast<uintptr_t>(sched) & 7) == 0;
+}
+
+ep_status_t combine_rank_major(const void* y, int hidden, const int64_t* topk_idx,
+                               const float* topk_weights, int64_t num_tokens, int num_topk,
+                               int num_experts, int num_ranks, const int32_t* slot, void* out,
+                               uint64_t* sched, int32_t* err_word, ep_stream_t stream) {
   if (!routing_ok(num_tokens, num_topk, num_experts, num_ranks)) return EP_ERR_INVALID_ARG;
   if (hidden < 8 || hidden % 8 != 0) return EP_ERR_INVALID_ARG;
   if (num_tokens == 0) return EP_OK;
   if (!y || !topk_idx || !slot || !out) return EP_ERR_INVALID_ARG;
-  if (!aligned16(y) || !aligned16(out)) return EP_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out) || !sched_ok(sched)) return EP_ERR_INVALID_ARG;
   DeviceProps props;
   if (!device_props(&props)) return EP_ERR_CUDA;
   Args a = {};
@@ -529,17 +599,19 @@ extern "C" ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk
   a.ll_slot = nullptr;
   a.err = err_word;
   a.dmax = num_topk < num_ranks ? num_topk : num_ranks;
+  a.sched = reinterpret_cast<unsigned long long*>(sched);
   return launch_combine(a, props, stream);
 }
 
-extern "C" ep_status_t ep_ll_combine(const void* y, int hidden, const float* topk_weights,
-                                     int64_t num_tokens, int num_topk, const int32_t* ll_slot,
-                                     void* out, int32_t* err_word, ep_stream_t stream) {
+ep_status_t combine_expert_major(const void* y, int hidden, const float* topk_weights,
+                                 int64_t num_tokens, int num_topk, const int32_t* ll_slot,
+                                 void* out, uint64_t* sched, int32_t* err_word,
+                                 ep_stream_t stream) {
   if (num_tokens < 0 || num_topk < 1 || num_topk > EP_MAX_TOPK) return EP_ERR_INVALID_ARG;
   if (hidden < 8 || hidden % 8 != 0) return EP_ERR_INVALID_ARG;
   if (num_tokens == 0) return EP_OK;
   if (!y || !ll_slot || !out) return EP_ERR_INVALID_ARG;
-  if (!aligned16(y) || !aligned16(out)) return EP_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out) || !sched_ok(sched)) return EP_ERR_INVALID_ARG;
   DeviceProps props;
   if (!device_props(&props)) return EP_ERR_CUDA;
   Args a = {};
@@ -552,7 +624,42 @@ extern "C" ep_status_t ep_ll_combine(const void* y, int hidden, const float* top
   a.ll_slot = ll_slot;
   a.err = err_word;
   a.dmax = num_topk;
+  a.sched = reinterpret_cast<unsigned long long*>(sched);
   return launch_combine(a, props, stream);
+}
+
+}  // namespace
+
+extern "C" ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk_idx,
+                                  const float* topk_weights, int64_t num_tokens, int num_topk,
+                                  int num_experts, int num_ranks, const int32_t* slot, void* out,
+                                  int32_t* err_word, ep_stream_t stream) {
+  return combine_rank_major(y, hidden, topk_idx, topk_weights, num_tokens, num_topk, num_experts,
+                            num_ranks, slot, out, nullptr, err_word, stream);
+}
+
+extern "C" ep_status_t ep_combine_sched(const void* y, int hidden, const int64_t* topk_idx,
+                                        const float* topk_weights, int64_t num_tokens,
+                                        int num_topk, int num_experts, int num_ranks,
+                                        const int32_t* slot, void* out, uint64_t* sched,
+                                        int32_t* err_word, ep_stream_t stream) {
+  return combine_rank_major(y, hidden, topk_idx, topk_weights, num_tokens, num_topk, num_experts,
+                            num_ranks, slot, out, sched, err_word, stream);
+}
+
+extern "C" ep_status_t ep_ll_combine(const void* y, int hidden, const float* topk_weights,
+                                     int64_t num_tokens, int num_topk, const int32_t* ll_slot,
+                                     void* out, int32_t* err_word, ep_stream_t stream) {
+  return combine_expert_major(y, hidden, topk_weights, num_tokens, num_topk, ll_slot, out,
+                              nullptr, err_word, stream);
+}
+
+extern "C" ep_status_t ep_ll_combine_sched(const void* y, int hidden, const float* topk_weights,
+                                           int64_t num_tokens, int num_topk,
+                                           const int32_t* ll_slot, void* out, uint64_t* sched,
+                                           int32_t* err_word, ep_stream_t stream) {
+  return combine_expert_major(y, hidden, topk_weights, num_tokens, num_topk, ll_slot, out, sched,
+                              err_word, stream);
 }
 
 extern "C" void ep_debug_set_combine_stall(int unit) { ep::g_stall_unit = unit; }

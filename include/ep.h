@@ -364,9 +364,43 @@ ep_status_t ep_ll_combine(const void* y, int hidden, const float* topk_weights,
                           int64_t num_tokens, int num_topk, const int32_t* ll_slot, void* out,
                           int32_t* err_word, ep_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Dynamically scheduled combine.  The combine grid is persistent, and its
+ * blocks take the tokens in batches of a few.  Each block's first batch is
+ * fixed.  ep_combine and ep_ll_combine hand out the rest statically (block b
+ * takes every grid-th batch).  The _sched forms below hand out the rest on
+ * demand from a counter in device memory, so a block that the memory system
+ * serves faster takes more batches, and all blocks finish together.  On one
+ * GB300 this took skewed routing (131072 tokens) from 1586 to 1550 us per
+ * layout -> dispatch -> combine step, and Mixtral-shaped routing from 978 to
+ * 945 us.  The outputs are identical: each token is summed in the same
+ * order whichever block takes it.
+ *
+ * sched (device, EP_COMBINE_SCHED_WORDS 64-bit words, 8-byte aligned): the
+ * counter state.  The caller zeroes it once after allocating it.  Every
+ * launch leaves it zero again when its last block exits, including a launch
+ * that ran out of a bounded wait.  So one state serves any number of
+ * launches in order on one stream, and inside a CUDA graph.  Two combines
+ * that can run at the same time (other streams, a graph replayed beside
+ * eager calls) need separate states: a shared state would split the tokens
+ * between them and leave both outputs incomplete.  A NULL sched is the
+ * static schedule of ep_combine.  Other arguments and errors: as
+ * ep_combine and ep_ll_combine.
+ * ------------------------------------------------------------------------ */
+#define EP_COMBINE_SCHED_WORDS 2
+
+ep_status_t ep_combine_sched(const void* y, int hidden, const int64_t* topk_idx,
+                             const float* topk_weights, int64_t num_tokens, int num_topk,
+                             int num_experts, int num_ranks, const int32_t* slot, void* out,
+                             uint64_t* sched, int32_t* err_word, ep_stream_t stream);
+ep_status_t ep_ll_combine_sched(const void* y, int hidden, const float* topk_weights,
+                                int64_t num_tokens, int num_topk, const int32_t* ll_slot,
+                                void* out, uint64_t* sched, int32_t* err_word,
+                                ep_stream_t stream);
+
 /*
- * Test hook for the bounded waits of the combine pipeline (ep_combine and
- * ep_ll_combine).  The next combine launched from this host thread leaves
+ * Test hook for the bounded waits of the combine pipeline (ep_combine,
+ * ep_ll_combine and their _sched forms).  The next combine launched from this host thread leaves
  * pipeline unit `unit` of CTA 0 unarmed, so the waits on it run out after
  * about 1 s.  The launch then reports EP_ERRBIT_TIMEOUT in the error word,
  * its output is incomplete, and it returns.  The hook is one-shot; -1

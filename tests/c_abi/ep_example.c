@@ -103,6 +103,21 @@ int main(void) {
   for (int t = 0; t < T; ++t)
     for (int h = 0; h < H; ++h) CHECK(out[t][h] == (t == 6 ? 0 : x[t][h]), "combined row");
 
+  /* the dynamically scheduled combine: counters zeroed once, zero again after each launch */
+  uint64_t* d_sched;
+  CUDA(cudaMalloc((void**)&d_sched, sizeof(uint64_t) * EP_COMBINE_SCHED_WORDS));
+  CUDA(cudaMemset(d_sched, 0, sizeof(uint64_t) * EP_COMBINE_SCHED_WORDS));
+  for (int rep = 0; rep < 2; ++rep) {
+    CUDA(cudaMemset(d_out, 0xFF, sizeof x));
+    EP(ep_combine_sched(d_recv, H, d_idx, d_w, T, K, E, R, d_slot, d_out, d_sched, d_err, NULL));
+    uint16_t out2[T][H];
+    uint64_t sched[EP_COMBINE_SCHED_WORDS];
+    CUDA(cudaMemcpy(out2, d_out, sizeof out2, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(sched, d_sched, sizeof sched, cudaMemcpyDeviceToHost));
+    CHECK(memcmp(out2, out, sizeof out) == 0, "scheduled combine");
+    CHECK(sched[0] == 0 && sched[1] == 0, "counters back to zero");
+  }
+
   printf("ok\n");
   return 0;
 }

@@ -169,6 +169,21 @@ def test_combine_rejects_bad_arguments_and_accepts_empty(eplib):
     assert eplib.ep_combine(None, 256, None, None, 0, 2, 8, 2, None, None, None, None) == 0
 
 
+def test_sched_combines_reject_bad_arguments_and_accept_empty(eplib):
+    p = C.c_void_p(4096)
+    ok_sched, bad_sched = C.c_void_p(8192), C.c_void_p(8196)  # the counters need 8-byte alignment
+    f = eplib.ep_combine_sched
+    assert f(p, 12, p, p, 8, 2, 8, 2, p, p, ok_sched, None, None) == EP_ERR_INVALID_ARG
+    assert f(p, 256, None, p, 8, 2, 8, 2, p, p, ok_sched, None, None) == EP_ERR_INVALID_ARG
+    assert f(p, 256, p, p, 8, 2, 8, 2, p, p, bad_sched, None, None) == EP_ERR_INVALID_ARG
+    assert f(None, 256, None, None, 0, 2, 8, 2, None, None, bad_sched, None, None) == 0
+    g = eplib.ep_ll_combine_sched
+    assert g(p, 12, p, 8, 2, p, p, ok_sched, None, None) == EP_ERR_INVALID_ARG
+    assert g(p, 256, p, 8, 2, None, p, ok_sched, None, None) == EP_ERR_INVALID_ARG
+    assert g(p, 256, p, 8, 2, p, p, bad_sched, None, None) == EP_ERR_INVALID_ARG
+    assert g(None, 256, None, 0, 2, None, None, None, None, None) == 0
+
+
 def test_binding_fails_loudly_without_the_library(tmp_path):
     import combine_get_dispatch_04_gb300 as ep
     saved = ep._lib

@@ -227,6 +227,8 @@ def test_combine_bounded_wait_reports_timeout_and_recovers(ep):
     elapsed = time.time() - t0
     assert int(err.item()) & ep.EP_ERRBIT_TIMEOUT
     assert elapsed < 10, elapsed
+    # the launch that timed out still returned its scheduling counters to zero
+    assert L.sched is not None and L.sched.tolist() == [0, 0]
     # the context is intact: a normal combine matches the oracle
     err.zero_()
     out = ep.combine(d.recv_x, idx, w, L, err=err)

@@ -1,0 +1,92 @@
+"""The dynamically scheduled combine (ep_combine_sched / ep_ll_combine_sched,
+used by the binding through each layout's counters) gives exactly the
+static schedule's output (ep_combine with no counters): every token is
+summed in the same order whichever block claims it.  The counters are zero
+after every launch, so one state serves back-to-back launches on a stream.
+Shapes cover one-token batches (768 tokens over 456 or 608 blocks),
+multi-token batches (many small rows), fewer tokens than blocks, and the
+unweighted rank sum."""
+from __future__ import annotations
+
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from ep_testlib import assert_combine_close, bits_of, combine_bound, device_inputs
+from workloads import Config, make_case
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    Config("sched_decode_like", 32, 24, 1024, 256, 8, seed=1201),
+    Config("sched_small_rows", 16, 2048, 256, 64, 6, routing="zipf", zipf_s=1.2, mask_prob=0.05,
+           seed=1202),
+    Config("sched_few_tokens", 4, 16, 1024, 16, 4, seed=1203),
+    Config("sched_two_experts", 8, 1024, 512, 8, 2, seed=1204),
+]
+
+
+def _recv_rows(L):
+    return int(L.recv_base[-1].item())
+
+
+@pytest.mark.parametrize("cfg", SHAPES, ids=lambda c: c.name)
+@pytest.mark.parametrize("weighted", [True, False])
+def test_scheduled_combine_equals_static(ep, cfg, weighted):
+    c = make_case(cfg)
+    idx, w, x = device_inputs(c)
+    E, R = cfg.num_experts, cfg.num_ranks
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L = ep.get_dispatch_layout(idx, E, R, err=err)
+    d = ep.dispatch(x, idx, w, L, err=err)
+    wt = w if weighted else None
+    assert L.sched is not None
+    dyn = ep.combine(d.recv_x, idx, wt, L, err=err)
+    static = ep.combine(d.recv_x, idx, wt, replace(L, sched=None), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    np.testing.assert_array_equal(bits_of(dyn), bits_of(static))
+    assert L.sched.tolist() == [0, 0]
+    if weighted:
+        P = _recv_rows(L)
+        slot = L.slot.cpu().numpy()
+        y = bits_of(d.recv_x[:P])
+        want = oracle.combine(y, c.topk_idx, c.topk_weights, E, R, slot)
+        bound = combine_bound(oracle.bf16_to_double(y), c.topk_idx, c.topk_weights, slot, E // R,
+                              np.arange(cfg.num_tokens))
+        assert_combine_close(bits_of(dyn), want, bound)
+
+
+def test_one_state_serves_back_to_back_launches(ep):
+    cfg = SHAPES[1]
+    c = make_case(cfg)
+    idx, w, x = device_inputs(c)
+    E, R = cfg.num_experts, cfg.num_ranks
+    L = ep.get_dispatch_layout(idx, E, R)
+    d = ep.dispatch(x, idx, w, L)
+    outs = [ep.combine(d.recv_x, idx, w, L) for _ in range(6)]  # no host sync in between
+    torch.cuda.synchronize()
+    first = bits_of(outs[0])
+    for o in outs[1:]:
+        np.testing.assert_array_equal(bits_of(o), first)
+    assert L.sched.tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("cfg", SHAPES[:2], ids=lambda c: c.name)
+def test_expert_major_scheduled_combine_equals_static(ep, cfg):
+    c = make_case(cfg)
+    idx, w, x = device_inputs(c)
+    E, R, T = cfg.num_experts, cfg.num_ranks, cfg.num_tokens
+    cap = max(1, int(oracle.ll_layout(c.topk_idx, E, R, T).ll_count.max()))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    LL = ep.ll_get_dispatch_layout(idx, E, R, cap, err=err)
+    y = torch.randn((LL.num_rows, cfg.hidden), device="cuda").to(torch.bfloat16)
+    dyn = ep.ll_combine(y, w, LL, err=err)
+    static = ep.ll_combine(y, w, replace(LL, sched=None), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    np.testing.assert_array_equal(bits_of(dyn), bits_of(static))
+    assert LL.sched.tolist() == [0, 0]

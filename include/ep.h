@@ -164,7 +164,7 @@ ep_status_t ep_get_dispatch_layout_path(const int64_t* topk_idx, int64_t num_tok
 
 /*
  * The same layout as ep_get_dispatch_layout, for callers that cannot
- * allocate device memory when they call it (the paper has no counterpart to
+ * allocate device memory when they call it (the MSCCL++ EP pages have no counterpart to
  * this entry point).  Such callers include plugin or custom-op hosts that
  * hand the library only tensors they already own, C callers with no device
  * allocator of their own, and serving loops whose device-memory budget is

@@ -176,7 +176,9 @@ class Layout:
     workspace: torch.Tensor | None = None
     # [2] int64 counters of the dynamically scheduled combine, zero between
     # launches; None: the static schedule.  One Layout's combines run in
-    # order on one stream (or in one graph), never two at once.
+    # order on one stream (or in one graph), never two at once; a combine
+    # that may overlap another takes a copy of the Layout with its own
+    # counters (dataclasses.replace(L, sched=alloc_combine_sched(device))).
     sched: torch.Tensor | None = None
 
     @property

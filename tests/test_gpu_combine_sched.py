@@ -5,7 +5,8 @@ summed in the same order whichever block claims it.  The counters are zero
 after every launch, so one state serves back-to-back launches on a stream.
 Shapes cover one-token batches (768 tokens over 456 or 608 blocks),
 multi-token batches (many small rows), fewer tokens than blocks, and the
-unweighted rank sum."""
+unweighted rank sum; and two streams combining through one layout at once,
+each with its own counters."""
 from __future__ import annotations
 
 from dataclasses import replace
@@ -90,3 +91,35 @@ def test_expert_major_scheduled_combine_equals_static(ep, cfg):
     assert int(err.item()) == 0
     np.testing.assert_array_equal(bits_of(dyn), bits_of(static))
     assert LL.sched.tolist() == [0, 0]
+
+
+def test_overlapping_combines_on_one_layout_with_their_own_counters(ep):
+    """Two streams combine different expert outputs through one layout at the
+    same time, the second with a copy of the layout that has its own
+    counters; each gets exactly its result alone."""
+    cfg = SHAPES[1]
+    c = make_case(cfg)
+    idx, w, x = device_inputs(c)
+    E, R = cfg.num_experts, cfg.num_ranks
+    L = ep.get_dispatch_layout(idx, E, R)
+    L2 = replace(L, sched=ep.alloc_combine_sched(idx.device))
+    rows = ep.worst_case_rows(cfg.num_tokens, cfg.num_topk, R)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77)
+    ys = [torch.randn((rows, cfg.hidden), device="cuda", generator=g).to(torch.bfloat16)
+          for _ in range(2)]
+    alone = [ep.combine(ys[0], idx, w, L), ep.combine(ys[1], idx, w, L)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    outs = [[], []]
+    for _ in range(3):
+        for i, lay in ((0, L), (1, L2)):  # interleave the two streams' launches
+            with torch.cuda.stream(streams[i]):
+                outs[i].append(ep.combine(ys[i], idx, w, lay))
+    torch.cuda.synchronize()
+    for i in (0, 1):
+        for o in outs[i]:
+            np.testing.assert_array_equal(bits_of(o), bits_of(alone[i]))
+    assert L.sched.tolist() == [0, 0] and L2.sched.tolist() == [0, 0]

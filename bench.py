@@ -13,6 +13,10 @@ overlap their copies, chunk by chunk).  Multi-GPU runs (torchrun) are independen
 GPU (the shuffle on one GPU has no cross-GPU step): per-GPU work is fixed,
 value = N * T / max-over-ranks step time.
 
+The default run (skewed routing) also times the other four workloads, each
+at its own size, and reports them under `workloads`: device step, per-kernel
+times and roofline fractions, and the clock window of each.
+
 `--impl reference` times the plain CPU oracle (the correctness reference)
 on the host cores on a bounded sample of the same workload.
 """
@@ -232,19 +236,21 @@ def cpu_baseline(case, target_s: float = 10.0) -> dict:
 
 
 # ----------------------------------------------------------------------------
-def config_dict(cfg: Config, P: int, cap: int, x_bytes: int) -> dict:
+def config_dict(cfg: Config, P: int, cap: int, x_bytes: int, flush: bool | None = None) -> dict:
     routing = "uniform distinct top-k" if cfg.routing == "uniform" else f"Zipf(s={cfg.zipf_s}) top-k"
     if cfg.mask_prob:
         routing += f", {int(round(cfg.mask_prob * 100))}% of slots masked"
+    if flush is None:
+        flush = needs_l2_flush(cfg, P)
     return {"workload": cfg.name, "num_ranks": cfg.num_ranks,
             "tokens_per_rank": cfg.tokens_per_rank, "num_tokens": cfg.num_tokens,
             "hidden": cfg.hidden, "num_experts": cfg.num_experts, "num_topk": cfg.num_topk,
             "routing": routing, "payload": "fp8_e4m3+scales" if cfg.fp8 else "bf16",
             "recv_rows": P, "recv_capacity_rows": cap, "seed": cfg.seed,
-            "l2": (f"inputs larger than L2 (x {x_bytes / 1e9:.2f} GB; receive buffer "
-                   f"{P * cfg.hidden * (1 if cfg.fp8 else 2) / 1e9:.2f} GB)"
-                   if x_bytes * 3 + P * cfg.hidden * 4 >= 2 * L2_BYTES else
-                   "L2 flushed between steps (256 MB write outside the per-step events)"),
+            "l2": ("L2 flushed between steps (a read of twice L2, outside the per-step events; "
+                   f"x is {x_bytes / 1e6:.1f} MB)" if flush else
+                   f"inputs larger than L2 (x {x_bytes / 1e9:.2f} GB; receive buffer "
+                   f"{P * cfg.hidden * (1 if cfg.fp8 else 2) / 1e9:.2f} GB)"),
             "experts": "identity (combine reads the dispatched rows)" if not cfg.fp8
                        else "random bf16 expert outputs"}
 
@@ -280,6 +286,383 @@ def run_reference(args, cfg: Config):
     print(json.dumps(line), flush=True)
 
 
+class StepRunner:
+    """One workload's device buffers and its step (layout -> dispatch ->
+    combine) through the public API; the token range [a, b) of dispatch and
+    combine serves the end-to-end pipeline's chunks."""
+
+    def __init__(self, ep, cfg: Config, rcfg: Config, args, dev, case):
+        import torch
+        self.ep, self.cfg, self.args, self.dev = ep, cfg, args, dev
+        T, H, K, R, E = cfg.num_tokens, cfg.hidden, cfg.num_topk, cfg.num_ranks, cfg.num_experts
+        self.T = T
+        self.idx = torch.from_numpy(case.topk_idx).to(dev)
+        self.w = torch.from_numpy(case.topk_weights).to(dev)
+        self.x = torch.from_numpy(case.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        self.out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.views = {}  # (a, b) -> the layout's rows of those tokens, made once
+        if args.layout == "ht":
+            # rank-major: worst-case capacity T * min(K, R) rows, no host sync per step
+            self.cap = ep.worst_case_rows(T, K, R)
+            self.L = ep.alloc_layout(T, E, R, dev)
+            self.D = ep.alloc_dispatched(self.cap, H, K, E, R, cfg.fp8, dev)
+            self.recv_rows = self.cap
+            recv_payload = self.D.recv_x
+        else:
+            # expert-major: T rows per expert (the worst case with distinct experts per
+            # token) when the buffers stay under 32 GB, else 1.25x the largest count
+            LL = ep.ll_get_dispatch_layout(self.idx, E, R, T)
+            torch.cuda.synchronize(dev)
+            max_count = int(LL.ll_count.max().item())
+            cap = T if E * T * H * 2 <= (32 << 30) else ((max_count * 5 // 4 + 63) // 64) * 64
+            self.L = ep.alloc_ll_layout(T, K, E, R, cap, dev)
+            self.do_layout()
+            self.D = ep.ll_dispatch(self.x, self.L, use_fp8=cfg.fp8, err=self.err)
+            self.recv_rows = E * cap
+            recv_payload = self.D.recv_x
+        if cfg.fp8:  # combine is bf16 in: random expert outputs in the receive layout
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(rcfg.seed)
+            self.Y = torch.randn((self.recv_rows, H), generator=gen, device=dev).to(torch.bfloat16)
+        else:
+            self.Y = recv_payload
+
+    def _view(self, a, b):
+        from dataclasses import replace
+        if (a, b) == (0, self.T):
+            return self.L
+        v = self.views.get((a, b))
+        if v is None:
+            L = self.L
+            if self.args.layout == "ht":
+                v = replace(L, slot=L.slot[a:b], is_token_in_rank=L.is_token_in_rank[a:b])
+            else:
+                v = replace(L, ll_slot=L.ll_slot[a:b])
+            self.views[(a, b)] = v
+        return v
+
+    def do_layout(self):
+        ep, cfg = self.ep, self.cfg
+        if self.args.layout == "ht":
+            ep.get_dispatch_layout(self.idx, cfg.num_experts, cfg.num_ranks, err=self.err,
+                                   out=self.L, path=self.args.layout_kernels)
+        else:
+            ep.ll_get_dispatch_layout(self.idx, cfg.num_experts, cfg.num_ranks, err=self.err,
+                                      out=self.L, path=self.args.layout_kernels)
+
+    def do_dispatch(self, a, b):
+        Lc = self._view(a, b)
+        if self.args.layout == "ht":
+            self.ep.dispatch(self.x[a:b], self.idx[a:b], self.w[a:b], Lc, use_fp8=self.cfg.fp8,
+                             err=self.err, out=self.D)
+        else:
+            self.ep.ll_dispatch(self.x[a:b], Lc, use_fp8=self.cfg.fp8, err=self.err, out=self.D)
+
+    def do_combine(self, a, b):
+        Lc = self._view(a, b)
+        if self.args.layout == "ht":
+            self.ep.combine(self.Y, self.idx[a:b], self.w[a:b], Lc, err=self.err,
+                            out=self.out[a:b])
+        else:
+            self.ep.ll_combine(self.Y, self.w[a:b], Lc, err=self.err, out=self.out[a:b])
+
+    def step(self, ev=None, per_kernel=True):
+        # ev[0] / ev[3] bracket the step; ev[1] / ev[2] (per_kernel) split it
+        # into layout, dispatch and combine
+        s = self.stream
+        if ev is not None:
+            ev[0].record(s)
+        self.do_layout()
+        if ev is not None and per_kernel:
+            ev[1].record(s)
+        self.do_dispatch(0, self.T)
+        if ev is not None and per_kernel:
+            ev[2].record(s)
+        self.do_combine(0, self.T)
+        if ev is not None:
+            ev[3].record(s)
+
+    def rows(self) -> int:
+        if self.args.layout == "ht":
+            return self.ep.total_rows(self.L)
+        return int(self.L.ll_count.sum().item())
+
+    def layout_launches(self):
+        ep, args, cfg = self.ep, self.args, self.cfg
+        T, K, R, E = cfg.num_tokens, cfg.num_topk, cfg.num_ranks, cfg.num_experts
+        if args.layout == "ll":
+            if args.layout_kernels == "single" or (args.layout_kernels == "auto"
+                                                   and ep.ll_auto_single_launch(T, K, R, E)):
+                return 1, "single"
+            return 3, "multi"  # rank, expert scan, assign
+        if args.layout_kernels == "single" or (args.layout_kernels == "auto"
+                                               and ep.auto_single_launch(T, R, E)):
+            return 1, "single"  # one thread-block cluster
+        # count + assign, with the scan folded in unless R * blocks > 8192 (T > 0)
+        nb = R * ((T // R + 511) // 512)
+        return (2 if R * nb <= 8192 else 3), "multi"
+
+
+def needs_l2_flush(cfg: Config, P: int) -> bool:
+    """Flush L2 between timed steps when the step's input rows fit in L2 (they
+    could stay resident from one step to the next) or the whole step moves
+    less than twice L2."""
+    x_bytes = cfg.num_tokens * cfg.hidden * 2
+    step_bytes = x_bytes * 3 + P * cfg.hidden * 2 * 2
+    return x_bytes < L2_BYTES or step_bytes < 2 * L2_BYTES
+
+
+def time_device(run: StepRunner, args, world: int, graph=None, min_region_s: float = 0.5):
+    """Timed passes of exactly K steps with the inputs resident in HBM.
+
+    The plain pass times K steps as a user runs them: no event between the
+    kernels, because an event recorded between two kernels stops the second
+    one's early (programmatic) launch, which costs several microseconds per
+    kernel edge.  It is repeated until the passes cover min_region_s (so
+    that the clock sampler sees the GPU under load), and the median pass is
+    reported.  One more pass puts an event around every kernel, for the
+    per-kernel durations (layout, dispatch, combine) that the roofline
+    uses; these include that lost overlap.  With an L2 flush (a read of a
+    buffer twice the size of L2, which leaves no dirty lines behind) between
+    steps, a pair of events brackets each step instead and the flush stays
+    outside them."""
+    import torch
+    import torch.distributed as dist
+    dev, stream, K = run.dev, run.stream, args.steps
+    P = run.rows()
+    flush = needs_l2_flush(run.cfg, P)
+    scrub = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+
+    def one_pass(per_kernel):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_start.record(stream)
+        for i in range(K):
+            if flush:
+                scrub.sum()
+            if graph is not None and not per_kernel:
+                if flush:
+                    evs[i][0].record(stream)
+                graph.replay()
+                if flush:
+                    evs[i][3].record(stream)
+            else:
+                run.step(evs[i] if (flush or per_kernel) else None, per_kernel=per_kernel)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        if flush:
+            step_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in evs)
+        else:
+            step_ms = t_start.elapsed_time(t_end) / K
+        return step_ms, evs
+
+    wall0 = time.time()
+    passes = []
+    while True:
+        ms, _ = one_pass(per_kernel=False)
+        passes.append(ms)
+        if time.time() - wall0 >= min_region_s or len(passes) >= 200:
+            break
+    ms_kernels, evs = one_pass(per_kernel=True)
+    wall1 = time.time()
+    return {
+        "P": P, "flush": flush, "ms": statistics.median(passes), "passes": passes,
+        "window": (wall0, wall1),
+        "ms_kernels": ms_kernels,
+        "layout_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+        "dispatch_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
+        "combine_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in evs),
+    }
+
+
+def link_bandwidth(dev, nbytes: int = 256 << 20) -> dict:
+    """Pinned host <-> device copy rates of this machine (GB/s), each direction
+    alone and both at once on two streams: the floor under `e2e`."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h2 = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d2 = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn, reps=3):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    def both():
+        with torch.cuda.stream(s1):
+            d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+
+    t_in = timed(lambda: d.copy_(h, non_blocking=True))
+    t_out = timed(lambda: h2.copy_(d2, non_blocking=True))
+    t_both = timed(both)
+    return {"h2d_gbs": nbytes / t_in / 1e9, "d2h_gbs": nbytes / t_out / 1e9,
+            "both_gbs": 2 * nbytes / t_both / 1e9, "bytes_per_copy": nbytes}
+
+
+def time_e2e(run: StepRunner, args, case, world: int) -> dict:
+    """The step through the public API on host buffers, pipelined over token
+    chunks: routing in -> layout; then per chunk, x in (copy stream) ->
+    dispatch + combine of that chunk's tokens (compute stream) -> out back
+    (second copy stream).  Every step moves all inputs in and the whole
+    result out.  Consecutive steps overlap their copies chunk by chunk."""
+    import torch
+    import torch.distributed as dist
+    dev, stream, T, H = run.dev, run.stream, run.T, run.cfg.hidden
+    h_idx = torch.from_numpy(case.topk_idx).pin_memory()
+    h_w = torch.from_numpy(case.topk_weights).pin_memory()
+    h_x = torch.from_numpy(case.x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    steps = max(1, min(args.steps, 20))
+    n_chunks = max(1, min(args.e2e_chunks, T // args.e2e_min_chunk_tokens))
+    bounds = [T * i // n_chunks for i in range(n_chunks + 1)]
+    chunks = [(bounds[c], bounds[c + 1]) for c in range(n_chunks)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(n_chunks)]      # x chunk landed
+    ev_used = [torch.cuda.Event() for _ in range(n_chunks)]    # x chunk read by dispatch
+    ev_done = [torch.cuda.Event() for _ in range(n_chunks)]    # out chunk computed
+    ev_back = [torch.cuda.Event() for _ in range(n_chunks)]    # out chunk copied back
+    x_dst = [run.x[a:b] for a, b in chunks]
+    x_src = [h_x[a:b] for a, b in chunks]
+    o_dst = [h_out[a:b] for a, b in chunks]
+    o_src = [run.out[a:b] for a, b in chunks]
+    first = [True]
+
+    def e2e_step():
+        # routing in and layout on the compute stream (after the previous
+        # step's kernels, which read idx and w)
+        run.idx.copy_(h_idx, non_blocking=True)
+        run.w.copy_(h_w, non_blocking=True)
+        with torch.cuda.stream(s_in):
+            for c in range(n_chunks):
+                if not first[0]:
+                    s_in.wait_event(ev_used[c])  # the previous step has read this x chunk
+                x_dst[c].copy_(x_src[c], non_blocking=True)
+                ev_in[c].record(s_in)
+        run.do_layout()
+        for c, (a, b) in enumerate(chunks):
+            stream.wait_event(ev_in[c])
+            run.do_dispatch(a, b)
+            ev_used[c].record(stream)
+            if not first[0]:
+                stream.wait_event(ev_back[c])  # the previous step's copy of this out chunk is done
+            run.do_combine(a, b)
+            ev_done[c].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[c])
+                o_dst[c].copy_(o_src[c], non_blocking=True)
+                ev_back[c].record(s_out)
+        first[0] = False
+
+    def e2e_drain():
+        for c in range(n_chunks):
+            stream.wait_event(ev_back[c])
+
+    e2e_step()
+    e2e_drain()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    h0 = time.perf_counter()
+    for _ in range(steps):
+        e2e_step()
+    e2e_drain()
+    host_s = time.perf_counter() - h0  # enqueueing only: the calls return before the GPU is done
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / steps, dev)
+    # the pipelined steps must give the resident step's result, bit for bit
+    run.step()
+    torch.cuda.synchronize(dev)
+    same = torch.equal(h_out.view(torch.int16), run.out.cpu().view(torch.int16))
+    h2d = h_idx.numel() * 8 + h_w.numel() * 4 + h_x.numel() * 2
+    d2h = h_out.numel() * 2
+    link = link_bandwidth(dev)
+    floor_ms = 1e3 * max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9),
+                         (h2d + d2h) / (link["both_gbs"] * 1e9))
+    return {"value": whole_job_tokens_per_s(T, world, e2e_ms), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+            "steps": steps, "token_chunks": n_chunks,
+            "host_enqueue_ms_per_step": 1e3 * host_s / steps,
+            "link": {k: round(v, 1) for k, v in link.items()},
+            "link_floor_ms": floor_ms,
+            "check": "out matches the device-resident step" if same else "MISMATCH"}
+
+
+def kernel_report(cfg: Config, P: int, t: dict, peak: float) -> dict:
+    ab = algorithmic_bytes(cfg, P)
+    kern = {
+        "layout": {"ms": t["layout_ms"], "bytes": ab["layout"]},
+        "dispatch": {"ms": t["dispatch_ms"], "bytes": ab["dispatch"]},
+        "combine": {"ms": t["combine_ms"], "bytes": ab["combine"]},
+    }
+    for k in ("dispatch", "combine"):
+        kern[k]["gbs"] = ab[k] / (kern[k]["ms"] / 1e3) / 1e9
+        kern[k]["frac"] = kern[k]["gbs"] / peak
+    return kern
+
+
+def other_workloads(args, ep, dev, peak: float) -> dict:
+    """The remaining workloads at their own sizes, each timed as the default
+    one (K steps, passes repeated to 0.3 s, median pass; one pass with
+    per-kernel events): device step, per-kernel times and roofline
+    fractions, and the clock window of each."""
+    import torch
+    out = {}
+    names = args.workload_list.split(",") if args.workload_list else list(CONFIGS)
+    for name in names:
+        if name == args.config:
+            continue
+        cfg = CONFIGS[name]
+        case = make_case(cfg)
+        run = StepRunner(ep, cfg, cfg, args, dev, case)
+        for _ in range(args.warmup):
+            run.step()
+        torch.cuda.synchronize(dev)
+        t = time_device(run, args, 1, min_region_s=0.3)
+        if int(run.err.item()) != 0:
+            raise SystemExit(f"{name}: device error word {int(run.err.item())}")
+        P = t["P"]
+        kern = kernel_report(cfg, P, t, peak)
+        ab = algorithmic_bytes(cfg, P)
+        launches, kinds = run.layout_launches()
+        out[name] = {
+            "tokens_per_s": whole_job_tokens_per_s(cfg.num_tokens, 1, t["ms"]),
+            "ms_per_step": t["ms"], "steps": args.steps, "passes": len(t["passes"]),
+            "hbm_gbs": (ab["dispatch"] + ab["combine"]) / (t["ms"] / 1e3) / 1e9,
+            "layout_ms": kern["layout"]["ms"], "layout_kernels": kinds,
+            "dispatch": {k: kern["dispatch"][k] for k in ("ms", "gbs", "frac")},
+            "combine": {k: kern["combine"][k] for k in ("ms", "gbs", "frac")},
+            "kernel_timing_ms_per_step": t["ms_kernels"],
+            "recv_rows": P, "dtype": "e4m3+bf16" if cfg.fp8 else "bf16",
+            "l2": "flushed between steps (read of 2x L2, outside the per-step events)"
+                  if t["flush"] else "inputs larger than L2",
+            "_window": t["window"], "gpu_launches": (launches + 2) * args.steps * len(t["passes"]),
+        }
+        del run, case
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, cfg: Config):
     import torch
     import torch.distributed as dist
@@ -301,262 +684,61 @@ def run_ours(args, cfg: Config):
 
     rcfg = replica_config(cfg, rank)
     case = make_case(rcfg)
-    T, H, K, R, E = cfg.num_tokens, cfg.hidden, cfg.num_topk, cfg.num_ranks, cfg.num_experts
-    idx = torch.from_numpy(case.topk_idx).to(dev)
-    w = torch.from_numpy(case.topk_weights).to(dev)
-    x = torch.from_numpy(case.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
-    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    from dataclasses import replace as _replace
-
-    if args.layout == "ht":
-        # rank-major: worst-case capacity T * min(K, R) rows, no host sync per step
-        cap = ep.worst_case_rows(T, K, R)
-        L = ep.alloc_layout(T, E, R, dev)
-        D = ep.alloc_dispatched(cap, H, K, E, R, cfg.fp8, dev)
-
-        def do_layout():
-            ep.get_dispatch_layout(idx, E, R, err=err, out=L, path=args.layout_kernels)
-
-        def do_dispatch(a, b):
-            Lc = L if (a, b) == (0, T) else _replace(
-                L, slot=L.slot[a:b], is_token_in_rank=L.is_token_in_rank[a:b])
-            ep.dispatch(x[a:b], idx[a:b], w[a:b], Lc, use_fp8=cfg.fp8, err=err, out=D)
-
-        def do_combine(a, b):
-            Lc = L if (a, b) == (0, T) else _replace(
-                L, slot=L.slot[a:b], is_token_in_rank=L.is_token_in_rank[a:b])
-            ep.combine(Y, idx[a:b], w[a:b], Lc, err=err, out=out[a:b])
-
-        recv_rows = cap
-        recv_payload = D.recv_x
-    else:
-        # expert-major: T rows per expert (the worst case with distinct experts per
-        # token) when the buffers stay under 32 GB, else 1.25x the largest count
-        LL = ep.ll_get_dispatch_layout(idx, E, R, T)
-        torch.cuda.synchronize(dev)
-        max_count = int(LL.ll_count.max().item())
-        cap = T if E * T * H * 2 <= (32 << 30) else ((max_count * 5 // 4 + 63) // 64) * 64
-        LL = ep.alloc_ll_layout(T, K, E, R, cap, dev)
-        DL = None
-
-        def do_layout():
-            ep.ll_get_dispatch_layout(idx, E, R, err=err, out=LL, path=args.layout_kernels)
-
-        def do_dispatch(a, b):
-            LLc = LL if (a, b) == (0, T) else _replace(LL, ll_slot=LL.ll_slot[a:b])
-            ep.ll_dispatch(x[a:b], LLc, use_fp8=cfg.fp8, err=err, out=DL)
-
-        def do_combine(a, b):
-            LLc = LL if (a, b) == (0, T) else _replace(LL, ll_slot=LL.ll_slot[a:b])
-            ep.ll_combine(Y, w[a:b], LLc, err=err, out=out[a:b])
-
-        do_layout()
-        DL = ep.ll_dispatch(x, LL, use_fp8=cfg.fp8, err=err)
-        recv_rows = E * cap
-        recv_payload = DL.recv_x
-
-    if cfg.fp8:  # combine is bf16 in: random expert outputs in the receive layout
-        gen = torch.Generator(device=dev)
-        gen.manual_seed(rcfg.seed)
-        Y = torch.randn((recv_rows, H), generator=gen, device=dev).to(torch.bfloat16)
-    else:
-        Y = recv_payload
-
-    def step(ev=None, per_kernel=True):
-        # ev[0] / ev[3] bracket the step; ev[1] / ev[2] (per_kernel) split it
-        # into layout, dispatch and combine
-        if ev is not None:
-            ev[0].record(stream)
-        do_layout()
-        if ev is not None and per_kernel:
-            ev[1].record(stream)
-        do_dispatch(0, T)
-        if ev is not None and per_kernel:
-            ev[2].record(stream)
-        do_combine(0, T)
-        if ev is not None:
-            ev[3].record(stream)
-
+    T = cfg.num_tokens
+    run = StepRunner(ep, cfg, rcfg, args, dev, case)
     for _ in range(args.warmup):
-        step()
+        run.step()
     torch.cuda.synchronize(dev)
-    P = ep.total_rows(L) if args.layout == "ht" else int(LL.ll_count.sum().item())
-    P_est = P
-    if int(err.item()) != 0:
-        raise SystemExit(f"device error word {int(err.item())} after warm-up")
+    if int(run.err.item()) != 0:
+        raise SystemExit(f"device error word {int(run.err.item())} after warm-up")
 
     graph = None
     if args.graph:  # every one-time set-up ran in the warm-up steps
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            step()
+            run.step()
         graph.replay()
         torch.cuda.synchronize(dev)
-
-    # ---------------- timed region: inputs resident in HBM ----------------
-    # Pass 1 times exactly K steps as a user runs them: no event between the
-    # kernels, because an event recorded between two kernels stops the second
-    # one's early (programmatic) launch, which costs several microseconds per
-    # kernel edge.  Pass 2 runs K more steps with an event around every
-    # kernel, for the per-kernel durations (layout, dispatch, combine) that the
-    # roofline uses; these include that lost overlap.
-    # Workloads that move less than twice L2 per step get L2 flushed between
-    # steps (a 256 MB write outside the per-step events); the others stream
-    # far more than L2 holds.
-    step_bytes = T * H * 2 * 3 + (P_est * H * 2 * 2)
-    flush = step_bytes < 2 * L2_BYTES
-    scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-
-    def timed_pass(per_kernel):
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-        t_start.record(stream)
-        for i in range(args.steps):
-            if flush:
-                scrub.fill_(i & 0xFF)
-            if graph is not None and not per_kernel:
-                if flush:
-                    evs[i][0].record(stream)
-                graph.replay()
-                if flush:
-                    evs[i][3].record(stream)
-            else:
-                step(evs[i] if (flush or per_kernel) else None, per_kernel=per_kernel)
-        t_end.record(stream)
-        torch.cuda.synchronize(dev)
-        if world > 1:
-            dist.barrier()
-        if flush:
-            step_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in evs)
-        else:
-            step_ms = t_start.elapsed_time(t_end) / args.steps
-        return step_ms, evs
 
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
     time.sleep(1.0)  # let nvidia-smi start sampling before the timed region
-    wall0 = time.time()
-    ms_local, _ = timed_pass(per_kernel=False)
-    ms_kernels_local, evs = timed_pass(per_kernel=True)
-    wall1 = time.time()
+    t = time_device(run, args, world, graph=graph)
+    ms = max_over_ranks(t["ms"], dev)
+    ms_with_kernel_events = max_over_ranks(t["ms_kernels"], dev)
+    P = t["P"]
+
+    e2e = time_e2e(run, args, case, world)
+    if int(run.err.item()) != 0:
+        raise SystemExit(f"device error word {int(run.err.item())}")
+    layout_launches, layout_kernels = run.layout_launches()
+    recv_rows = run.recv_rows
+    del run
+    torch.cuda.empty_cache()
+
+    peak, peak_kind = load_peaks()
+    block = None
+    if rank == 0 and world == 1 and args.workloads:
+        block = other_workloads(args, ep, dev, peak)
     sampler.stop()
-    ms = max_over_ranks(ms_local, dev)
-    ms_with_kernel_events = max_over_ranks(ms_kernels_local, dev)
-    lay_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    dis_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    com_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    clocks = sampler.summary(wall0, wall1)
-    clocks["timed_region_s"] = round(wall1 - wall0, 3)
 
-    # ---------------- end to end: pinned host buffers, copies timed --------
-    h_idx = torch.from_numpy(case.topk_idx).pin_memory()
-    h_w = torch.from_numpy(case.topk_weights).pin_memory()
-    h_x = torch.from_numpy(case.x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    e2e_steps = max(1, min(args.steps, 20))
-    # The step through the public API on host buffers, pipelined over token
-    # chunks: routing in -> layout; then per chunk, x in (copy stream) ->
-    # dispatch + combine of that chunk's tokens (compute stream) -> out back
-    # (second copy stream).  Every step moves all inputs in and the whole
-    # result out.
-    n_chunks = max(1, min(args.e2e_chunks, T // args.e2e_min_chunk_tokens))
-    bounds = [T * i // n_chunks for i in range(n_chunks + 1)]
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(n_chunks)]      # x chunk landed
-    ev_used = [torch.cuda.Event() for _ in range(n_chunks)]    # x chunk read by dispatch
-    ev_done = [torch.cuda.Event() for _ in range(n_chunks)]    # out chunk computed
-    ev_back = [torch.cuda.Event() for _ in range(n_chunks)]    # out chunk copied back
-    first = [True]
+    def clocks_of(window):
+        c = sampler.summary(*window)
+        c["timed_region_s"] = round(window[1] - window[0], 3)
+        return c
 
-    def e2e_step():
-        # routing in and layout on the compute stream (after the previous
-        # step's kernels, which read idx and w)
-        idx.copy_(h_idx, non_blocking=True)
-        w.copy_(h_w, non_blocking=True)
-        for c in range(n_chunks):
-            a, b = bounds[c], bounds[c + 1]
-            with torch.cuda.stream(s_in):
-                if not first[0]:
-                    s_in.wait_event(ev_used[c])  # the previous step has read this x chunk
-                x[a:b].copy_(h_x[a:b], non_blocking=True)
-                ev_in[c].record(s_in)
-        do_layout()
-        for c in range(n_chunks):
-            a, b = bounds[c], bounds[c + 1]
-            stream.wait_event(ev_in[c])
-            do_dispatch(a, b)
-            ev_used[c].record(stream)
-            if not first[0]:
-                stream.wait_event(ev_back[c])  # the previous step's copy of this out chunk is done
-            do_combine(a, b)
-            ev_done[c].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_done[c])
-                h_out[a:b].copy_(out[a:b], non_blocking=True)
-                ev_back[c].record(s_out)
-        first[0] = False
-
-    def e2e_drain():
-        for c in range(n_chunks):
-            stream.wait_event(ev_back[c])
-
-    e2e_step()
-    e2e_drain()
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e2e_drain()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
-    # the pipelined steps must give the resident step's result, bit for bit
-    step()
-    torch.cuda.synchronize(dev)
-    e2e_check = "out matches the device-resident step" if torch.equal(
-        h_out.view(torch.int16), out.cpu().view(torch.int16)) else "MISMATCH"
-    h2d = h_idx.numel() * 8 + h_w.numel() * 4 + h_x.numel() * 2
-    d2h = h_out.numel() * 2
-    if int(err.item()) != 0:
-        raise SystemExit(f"device error word {int(err.item())}")
-
-    layout_kernels = None
-    if args.layout == "ll":
-        if args.layout_kernels == "single" or (args.layout_kernels == "auto"
-                                               and ep.ll_auto_single_launch(T, K, R, E)):
-            layout_launches, layout_kernels = 1, "single"
-        else:
-            layout_launches, layout_kernels = 3, "multi"  # rank, expert scan, assign
-    elif args.layout_kernels == "single" or (args.layout_kernels == "auto"
-                                             and ep.auto_single_launch(T, R, E)):
-        layout_launches, layout_kernels = 1, "single"  # one thread-block cluster
-    else:  # count + assign, with the scan folded in unless R * blocks > 8192 (T > 0)
-        nb = R * ((T // R + 511) // 512)
-        layout_launches, layout_kernels = (2 if R * nb <= 8192 else 3), "multi"
+    clocks = clocks_of(t["window"])
+    if block is not None:
+        for name in block:
+            block[name]["clocks"] = clocks_of(block[name].pop("_window"))
     if rank == 0:
-        peak, peak_kind = load_peaks()
         ab = algorithmic_bytes(cfg, P)
         gbs = (ab["dispatch"] + ab["combine"]) / (ms / 1e3) / 1e9
-        kern = {
-            "layout": {"ms": lay_ms, "bytes": ab["layout"], "launches_per_step": layout_launches},
-            "dispatch": {"ms": dis_ms, "bytes": ab["dispatch"], "launches_per_step": 1,
-                         "gbs": ab["dispatch"] / (dis_ms / 1e3) / 1e9},
-            "combine": {"ms": com_ms, "bytes": ab["combine"], "launches_per_step": 1,
-                        "gbs": ab["combine"] / (com_ms / 1e3) / 1e9},
-        }
-        for k in ("dispatch", "combine"):
-            kern[k]["frac"] = kern[k]["gbs"] / peak
-        dom = "dispatch" if dis_ms >= com_ms else "combine"
+        kern = kernel_report(cfg, P, t, peak)
+        kern["layout"]["launches_per_step"] = layout_launches
+        kern["dispatch"]["launches_per_step"] = 1
+        kern["combine"]["launches_per_step"] = 1
+        dom = "dispatch" if kern["dispatch"]["ms"] >= kern["combine"]["ms"] else "combine"
         kname = {"dispatch": "dispatch_kernel", "combine": "combine_kernel"}[dom]
         src = {"dispatch": "ep_dispatch.cu", "combine": "ep_combine.cu"}[dom]
         # expert-major runs have their own captures ("<workload>/ll")
@@ -568,7 +750,8 @@ def run_ours(args, cfg: Config):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3+bf16" if cfg.fp8 else "bf16",
             "data": "synthetic (seeded routing and N(0,1) hidden states; no dataset)",
-            "config": dict(config_dict(cfg, P, recv_rows, T * H * 2), layout=args.layout,
+            "config": dict(config_dict(cfg, P, recv_rows, T * cfg.hidden * 2, t["flush"]),
+                           layout=args.layout,
                            **({"step_launch": "cuda_graph_replay"} if graph is not None else {}),
                            **({"layout_kernels": layout_kernels} if layout_kernels else {})),
             "hbm_gbs": gbs, "hbm_frac": gbs / peak, "peak_gbs": peak, "peak_kind": peak_kind,
@@ -578,18 +761,20 @@ def run_ours(args, cfg: Config):
                          "algorithmic_bytes_per_launch": ab[dom],
                          "peak_note": f"of {peak_kind} (copy bandwidth)"},
             "kernels": kern,
+            "passes": {"n": len(t["passes"]), "steps_each": args.steps,
+                       "ms_min": min(t["passes"]), "ms_max": max(t["passes"]),
+                       "note": "value and ms_per_step come from the median pass"},
             "kernel_timing": {"steps": args.steps, "ms_per_step": ms_with_kernel_events,
-                              "note": "per-kernel events in a second pass of K steps; an event "
+                              "note": "per-kernel events in one more pass of K steps; an event "
                                       "between two kernels stops the early launch of the second, "
                                       "so these steps run slower than the plain ones"},
-            "e2e": {"value": whole_job_tokens_per_s(T, world, e2e_ms), "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "steps": e2e_steps, "token_chunks": n_chunks,
-                    "check": e2e_check},
-            "gpu_launches": (layout_launches + 2) * args.steps,
+            "e2e": e2e,
+            "gpu_launches": (layout_launches + 2) * args.steps * len(t["passes"]),
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
+        if block is not None:
+            line["workloads"] = block
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -616,6 +801,12 @@ def main(argv=None):
                     help="time the plain steps as replays of one CUDA graph of the step "
                          "(no host launch cost; the per-kernel pass stays eager)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workloads", dest="workloads", action="store_true", default=None,
+                    help="also time the other workloads (default: on for the default run)")
+    ap.add_argument("--no-workloads", dest="workloads", action="store_false")
+    ap.add_argument("--workload-list", default=None,
+                    help="comma-separated workloads for the `workloads` block (default: all "
+                         "but --config)")
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="token chunks the end-to-end step pipelines its copies over")
     ap.add_argument("--e2e-min-chunk-tokens", type=int, default=2048,
@@ -625,6 +816,9 @@ def main(argv=None):
     if args.warmup < 3:
         args.warmup = 3
     cfg = CONFIGS[args.config]
+    if args.workloads is None:  # the default run carries every workload in its line
+        args.workloads = (args.config == DEFAULT_CONFIG and not args.tokens_per_rank
+                          and args.seed is None and args.layout == "ht" and not args.graph)
     if args.tokens_per_rank:
         cfg = cfg.scaled(args.tokens_per_rank)
     if args.seed is not None:

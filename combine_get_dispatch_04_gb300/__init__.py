@@ -27,6 +27,7 @@ EP_OK = 0
 EP_ERRBIT_BAD_EXPERT = 1
 EP_ERRBIT_CAPACITY = 2
 EP_ERRBIT_TIMEOUT = 4
+EP_ERRBIT_SCHED = 8
 EP_MAX_RANKS = 64
 EP_MAX_TOPK = 32
 EP_MAX_EXPERTS = 4096
@@ -115,7 +116,8 @@ _debug = os.environ.get("EP_DEBUG", "0") not in ("", "0")
 
 _ERRBITS = ((EP_ERRBIT_BAD_EXPERT, "an expert id outside [-1, E)"),
             (EP_ERRBIT_CAPACITY, "a row at or beyond the receive capacity"),
-            (EP_ERRBIT_TIMEOUT, "a bounded pipeline wait ran out"))
+            (EP_ERRBIT_TIMEOUT, "a bounded pipeline wait ran out"),
+            (EP_ERRBIT_SCHED, "a combine's scheduling counters were in use by another launch"))
 
 
 def set_debug(on: bool) -> None:
@@ -175,10 +177,10 @@ class Layout:
     num_ranks: int
     workspace: torch.Tensor | None = None
     # [2] int64 counters of the dynamically scheduled combine, zero between
-    # launches; None: the static schedule.  One Layout's combines run in
-    # order on one stream (or in one graph), never two at once; a combine
-    # that may overlap another takes a copy of the Layout with its own
-    # counters (dataclasses.replace(L, sched=alloc_combine_sched(device))).
+    # launches; None: the static schedule.  They serve the combines of the
+    # first stream that uses them; combines on any other stream get counters
+    # of their own (sched_for), so that combines through one Layout on two
+    # streams, or a graph replayed beside eager calls, never share them.
     sched: torch.Tensor | None = None
 
     @property
@@ -318,13 +320,28 @@ def dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor
     return out
 
 
-def _sched_of(layout, device: torch.device) -> torch.Tensor | None:
+def sched_for(layout, device: torch.device) -> torch.Tensor | None:
+    """The scheduling counters that a combine through `layout` on the current
+    stream uses.  The layout's own counters belong to the first stream that
+    uses them (recorded on the tensor, so copies of the Layout agree); a
+    combine on any other stream gets counters kept for that stream, zeroed
+    when first needed.  None: the layout asks for the static schedule."""
     s = layout.sched
-    if s is not None:
-        _need(s, "sched", torch.int64, (COMBINE_SCHED_WORDS,))
-        if s.device != device:
-            raise EPError("the layout's sched must be on the combine's device")
-    return s
+    if s is None:
+        return None
+    _need(s, "sched", torch.int64, (COMBINE_SCHED_WORDS,))
+    if s.device != device:
+        raise EPError("the layout's sched must be on the combine's device")
+    key = torch.cuda.current_stream(device).cuda_stream
+    home = getattr(s, "_ep_home_stream", None)
+    if home is None:
+        s._ep_home_stream = home = key
+    if key == home:
+        return s
+    others = s.__dict__.setdefault("_ep_other_streams", {})
+    if key not in others:
+        others[key] = alloc_combine_sched(device)
+    return others[key]
 
 
 def combine(y: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor | None,
@@ -346,7 +363,7 @@ def combine(y: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor 
     _need(out, "out", torch.bfloat16, (T, H))
     if err is not None:
         _need(err, "err", torch.int32)
-    sched = _sched_of(layout, y.device)
+    sched = sched_for(layout, y.device)
     _check(lib().ep_combine_sched(_ptr(y), H, _ptr(topk_idx), _ptr(topk_weights), T, K, E, R,
                                   _ptr(layout.slot), _ptr(out), _ptr(sched), _ptr(err),
                                   _stream(y.device)), "ep_combine_sched")
@@ -477,7 +494,7 @@ def ll_combine(y: torch.Tensor, topk_weights: torch.Tensor | None, layout: LLLay
     _need(out, "out", torch.bfloat16, (T, H))
     if err is not None:
         _need(err, "err", torch.int32)
-    sched = _sched_of(layout, y.device)
+    sched = sched_for(layout, y.device)
     _check(lib().ep_ll_combine_sched(_ptr(y), H, _ptr(topk_weights), T, K, _ptr(layout.ll_slot),
                                      _ptr(out), _ptr(sched), _ptr(err), _stream(y.device)),
            "ep_ll_combine_sched")

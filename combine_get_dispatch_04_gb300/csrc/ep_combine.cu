@@ -80,6 +80,7 @@ struct Args {
   int stall_unit;  // test hook: CTA 0 never arms this pipeline unit (-1: off)
   unsigned long long* sched;  // [2] claimed-batch and exited-block counters (null: static batches)
   int claim;                  // tokens per batch
+  int64_t nbatches;           // ceil(T / claim): the claims one launch makes when it runs alone
 };
 
 // Offsets of the shared-memory regions that follow the S row tiles.
@@ -276,6 +277,8 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
   int64_t* tT0 = reinterpret_cast<int64_t*>(smem + lay.hdr);      // [2] first token of the batch
   int32_t* tN = reinterpret_cast<int32_t*>(tT0 + 2);              // [2] its tokens (0: no more)
   volatile int* abort = reinterpret_cast<volatile int*>(smem + lay.abort);
+  uint32_t* nclaims = reinterpret_cast<uint32_t*>(smem + lay.abort + 4);  // this CTA's claims
+  uint32_t* overclaim = nclaims + 1;  // a claim beyond what a lone launch hands out
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
@@ -288,6 +291,8 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
       mbar_init(&tempty[b], kConsumerWarps);
     }
     *abort = 0;
+    *nclaims = 0;
+    *overclaim = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -302,12 +307,19 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
   if (warp == 1) {
     // ------------------------------------------------------------ routing
     bool ok = true, bad = false;
+    uint32_t claims = 0;
+    bool over = false;
     int64_t t0 = (int64_t)blockIdx.x * claim;
     for (uint32_t bi = 0;; ++bi) {
       const int buf = bi & 1;
       const uint32_t use = bi >> 1;
       unsigned long long nxt = 0;  // the next batch, claimed before it is needed
-      if (a.sched && t0 < a.T && lane == 0) nxt = atomicAdd(a.sched, (unsigned long long)claim);
+      if (a.sched && t0 < a.T && lane == 0) {
+        nxt = atomicAdd(a.sched, (unsigned long long)claim);
+        ++claims;
+        // a launch alone hands out exactly nbatches claims, 0 .. nbatches-1
+        over |= nxt >= (unsigned long long)a.nbatches * (unsigned long long)claim;
+      }
       if (use > 0 && !wait_warp(&tempty[buf], (use - 1) & 1, abort)) {
         ok = false;
         break;
@@ -326,6 +338,10 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
       t0 = a.sched ? dyn0 + (int64_t)__shfl_sync(0xFFFFFFFFu, nxt, 0) : t0 + dyn0;
     }
     if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && a.err) atomicOr(a.err, EP_ERRBIT_BAD_EXPERT);
+    if (lane == 0) {
+      *nclaims = claims;
+      *overclaim = over ? 1u : 0u;
+    }
     if (!ok && lane == 0) {
       *abort = 1;
       if (a.err) atomicOr(a.err, EP_ERRBIT_TIMEOUT);
@@ -429,16 +445,35 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
     }
   }
   // The last block to leave resets the counters for the next launch: every
-  // block has stopped claiming by then.
+  // block has stopped claiming by then.  sched[1] packs the blocks that have
+  // left (bits 0..31), the claims they made (bits 32..62) and whether any of
+  // them ran out of a bounded wait (bit 63).  A launch that had the counters
+  // to itself, from zero, leaves with exactly nbatches claims and
+  // sched[0] == nbatches * claim, every claim below that and every exit index
+  // below gridDim.x.  Anything else means that another launch shared the
+  // counters, or that they were not zero at launch: some tokens may have been
+  // skipped, so the launch reports EP_ERRBIT_SCHED.
   if (!a.sched) return;
   __syncthreads();
   if (threadIdx.x == 0) {
+    constexpr unsigned long long kLeft = 0xFFFFFFFFull, kAbort = 1ull << 63;
+    const unsigned long long mine =
+        1ull + ((unsigned long long)*nclaims << 32) + (*abort ? kAbort : 0ull);
     __threadfence();
-    if (atomicAdd(a.sched + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
+    const unsigned long long prev = atomicAdd(a.sched + 1, mine);
+    bool shared = *overclaim != 0 || (prev & kLeft) >= (unsigned long long)gridDim.x;
+    if ((prev & kLeft) == (unsigned long long)gridDim.x - 1) {
       __threadfence();
+      const unsigned long long all = prev + mine;
+      const unsigned long long claimed = *reinterpret_cast<volatile unsigned long long*>(a.sched);
+      // a launch that timed out loses claims on purpose: it reports EP_ERRBIT_TIMEOUT
+      if (!(all & kAbort))
+        shared |= ((all >> 32) & 0x7FFFFFFFull) != (unsigned long long)a.nbatches ||
+                  claimed != (unsigned long long)a.nbatches * (unsigned long long)a.claim;
       a.sched[0] = 0;
       a.sched[1] = 0;
     }
+    if (shared && a.err) atomicOr(a.err, EP_ERRBIT_SCHED);
   }
 }
 
@@ -558,6 +593,7 @@ ep_status_t launch_combine(Args& a, const DeviceProps& props, ep_stream_t stream
       (int64_t)props.sm_count * (resident < plan.ctas_per_sm ? resident : plan.ctas_per_sm);
   a.claim = claim_tokens(a.T, ctas, a.H, a.dmax);
   const int64_t batches = (a.T + a.claim - 1) / a.claim;
+  a.nbatches = batches;
   const int64_t grid = batches < ctas ? batches : ctas;
   launch_pdl(kernel, (unsigned)grid, kThreads, plan.smem, to_cuda(stream), a);
   return launch_status();

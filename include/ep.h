@@ -66,6 +66,8 @@ typedef enum {
 #define EP_ERRBIT_BAD_EXPERT 1 /* a topk_idx entry outside [-1, E): treated as masked */
 #define EP_ERRBIT_CAPACITY 2   /* a slot >= recv_capacity_rows: that row was not written */
 #define EP_ERRBIT_TIMEOUT 4    /* a bounded shared-memory pipeline wait ran out */
+#define EP_ERRBIT_SCHED 8      /* a scheduled combine found its counters in use by another
+                                  launch, or not zero at launch: tokens may be missing */
 
 #define EP_MAX_RANKS 64
 #define EP_MAX_TOPK 32
@@ -174,7 +176,9 @@ ep_status_t ep_get_dispatch_layout_path(const int64_t* topk_idx, int64_t num_tok
  * exits; nothing is allocated or freed.
  *
  * Arguments, outputs and error word: as ep_get_dispatch_layout, without the
- * workspace.  Returns EP_ERR_CAPACITY, with nothing enqueued, when
+ * workspace.  It always runs the multi-launch form (EP_LAYOUT_MULTI_LAUNCH),
+ * whatever the batch size; the outputs are the same as those of every other
+ * form.  Returns EP_ERR_CAPACITY, with nothing enqueued, when
  * ep_workspace_bytes(T, R, E) exceeds EP_NOALLOC_SCRATCH_BYTES (about 8 bytes
  * per token plus a small per-block term: roughly 800k tokens at 256 experts).
  * The first call on each device looks up the array's device address
@@ -383,9 +387,15 @@ ep_status_t ep_ll_combine(const void* y, int hidden, const float* topk_weights,
  * launches in order on one stream, and inside a CUDA graph.  Two combines
  * that can run at the same time (other streams, a graph replayed beside
  * eager calls) need separate states: a shared state would split the tokens
- * between them and leave both outputs incomplete.  A NULL sched is the
- * static schedule of ep_combine.  Other arguments and errors: as
- * ep_combine and ep_ll_combine.
+ * between them and leave both outputs incomplete.  A launch checks, as its
+ * blocks leave, that it made exactly the claims a launch alone makes and
+ * that no claim or exit came from elsewhere; if not (a shared state, or one
+ * that was not zero at launch) it sets EP_ERRBIT_SCHED in err_word, and its
+ * output may be missing tokens.  A shared state is not always caught (a
+ * launch that runs entirely between the other's claims sees nothing amiss,
+ * but then neither output is affected).  A NULL sched is the static
+ * schedule of ep_combine.  Other arguments and errors: as ep_combine and
+ * ep_ll_combine.
  * ------------------------------------------------------------------------ */
 #define EP_COMBINE_SCHED_WORDS 2
 

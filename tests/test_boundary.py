@@ -49,7 +49,7 @@ def test_status_strings(eplib):
 
 def test_workspace_bytes(eplib):
     wb = eplib.ep_workspace_bytes
-    assert wb(0, 4, 16) > 0 or wb(0, 4, 16) == wb(0, 4, 16)  # valid, possibly tiny
+    assert wb(0, 4, 16) == 0  # an empty batch needs no scratch
     assert wb(131072, 16, 64) >= 131072 * 8  # one 64-bit rank mask per token
     assert wb(512, 4, 16) <= wb(1024, 4, 16)
     assert wb(10, 4, 16) == 0   # T % R != 0
@@ -57,6 +57,21 @@ def test_workspace_bytes(eplib):
     assert wb(512, 65, 65) == 0  # R above the maximum
     assert wb(512, 4, 4100) == 0  # E above the maximum
     assert wb(-4, 4, 16) == 0
+
+
+def _expected_workspace(T, R, E):
+    """One 8-byte rank mask per token, then per 512-token block (blocks never
+    straddle two source ranks) R counts, R offsets and E expert counts, each
+    array padded to 256 bytes."""
+    pad = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    nb = R * ((T // R + 511) // 512)
+    return pad(8 * T) + 2 * pad(4 * R * nb) + pad(4 * nb * E)
+
+
+@pytest.mark.parametrize("T,R,E", [(512, 4, 16), (4096, 32, 256), (131072, 16, 64),
+                                   (1000, 1, 3), (4096, 64, 128)])
+def test_workspace_bytes_exact(eplib, T, R, E):
+    assert eplib.ep_workspace_bytes(T, R, E) == _expected_workspace(T, R, E)
 
 
 def _layout_call(eplib, T=8, K=2, E=8, R=2, ptrs=True, ws_bytes=1 << 20):

@@ -40,8 +40,13 @@ def test_bench_line_on_the_small_workload(ep, layout, graph):
     assert e2e["h2d_bytes_per_step"] == T * K * 8 + T * K * 4 + T * H * 2
     assert e2e["d2h_bytes_per_step"] == T * H * 2
     assert e2e["check"] == "out matches the device-resident step"
-    # one single-launch layout, dispatch and combine per step
-    assert d["gpu_launches"] == 3 * d["steps"]
+    assert e2e["link"]["h2d_gbs"] > 0 and e2e["link"]["d2h_gbs"] > 0
+    assert 0 < e2e["link_floor_ms"] and e2e["host_enqueue_ms_per_step"] > 0
+    # one single-launch layout, dispatch and combine per step, in every timed pass
+    assert d["passes"]["n"] >= 1 and d["passes"]["steps_each"] == 5
+    assert d["passes"]["ms_min"] <= d["ms_per_step"] <= d["passes"]["ms_max"]
+    assert d["gpu_launches"] == 3 * d["steps"] * d["passes"]["n"]
+    assert "workloads" not in d  # only the default run carries the other workloads
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     # the per-kernel times come from a second pass of the same number of steps
     kt = d["kernel_timing"]
@@ -52,3 +57,22 @@ def test_bench_line_on_the_small_workload(ep, layout, graph):
     if layout == "ht":
         cb = d["cpu_baseline"]
         assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
+
+
+def test_bench_workloads_block(ep):
+    """The block of other workloads that the default run adds to its line,
+    here with the decode FP8 workload beside the small one: each entry has
+    its step, per-kernel fractions against the same peak, and a clock window."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--config", "tiny", "--steps", "5",
+           "--warmup", "3", "--no-cpu-baseline", "--workloads", "--workload-list",
+           "decode_fp8,tiny"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][0])
+    assert list(d["workloads"]) == ["decode_fp8"]
+    w = d["workloads"]["decode_fp8"]
+    assert w["ms_per_step"] > 0 and w["tokens_per_s"] == pytest.approx(4096 / (w["ms_per_step"] / 1e3))
+    for k in ("dispatch", "combine"):
+        assert w[k]["frac"] == pytest.approx(w[k]["gbs"] / d["peak_gbs"])
+    assert w["l2"].startswith("flushed")  # x (58.7 MB) fits in L2
+    assert w["clocks"]["samples"] >= 1 and w["dtype"] == "e4m3+bf16"

@@ -163,6 +163,59 @@ def test_combine_full_size(ep, name):
         assert not out2[~live].view(torch.int16).any()
 
 
+@pytest.mark.parametrize("name", ["dsv3_prefill", "skewed"])
+def test_combine_full_batch_weighted_vs_oracle(ep, name):
+    """Every token of a full-size workload against the oracle, under the
+    workload's own (softmax, partly masked) weights and random expert outputs,
+    so that each destination rank's row differs: a wrong row, or a wrong
+    merge of the weights of slots that share a rank, shows up.  The oracle
+    runs once over the whole batch; the tolerance is checked on the device in
+    token chunks."""
+    cfg = CONFIGS[name]
+    c, want_layout = full_case(name)
+    idx, w, _ = device_inputs(c)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L = ep.get_dispatch_layout(idx, cfg.num_experts, cfg.num_ranks, err=err)
+    P = want_layout.num_rows
+    y_bits = workloads.signed_unit_bf16_bits(P, cfg.hidden, seed=cfg.seed + 40)
+    y = bf16_from_bits(y_bits)
+    out = torch.full((cfg.num_tokens, cfg.hidden), float("nan"), dtype=torch.bfloat16,
+                     device="cuda")
+    ep.combine(y, idx, w, L, err=err, out=out)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    np.testing.assert_array_equal(L.slot.cpu().numpy(), want_layout.slot)
+    want = oracle.combine(y_bits, c.topk_idx, c.topk_weights, cfg.num_experts, cfg.num_ranks,
+                          want_layout.slot)
+    del y_bits
+    El = cfg.num_experts // cfg.num_ranks
+    slot = L.slot.long()
+    T, K = c.topk_idx.shape
+    n_same = 0
+    for a in range(0, T, 8192):
+        b = min(T, a + 8192)
+        # sum_k |w_k y_k| per element, for the tolerance's cancellation guard
+        bound = torch.zeros((b - a, cfg.hidden), dtype=torch.float64, device="cuda")
+        ar = torch.arange(b - a, device="cuda")
+        for k in range(K):
+            e = idx[a:b, k]
+            live = (e >= 0) & (e < cfg.num_experts)
+            rows = slot[a:b][ar, torch.where(live, e // El, 0)]
+            term = w[a:b, k].double().abs()[:, None] * y[rows.clamp(min=0)].double().abs()
+            bound += torch.where(live[:, None], term, 0.0)
+        g = out[a:b].double()
+        r_bits = torch.from_numpy(want[a:b].view(np.int16)).cuda()
+        r = r_bits.view(torch.bfloat16).double()
+        assert bool(torch.isfinite(g).all())
+        excess = (g - r).abs() - 1e-2 * (r.abs() + bound)
+        assert not bool((excess > 0).any()), (
+            f"tokens [{a}, {b}): {int((excess > 0).sum())} elements out of tolerance, "
+            f"worst excess {float(excess.max()):.3e}")
+        n_same += int((out[a:b].view(torch.int16) == r_bits).sum())
+    # float32 FMA against a float64 sum: nearly every element rounds the same
+    assert n_same >= 0.9 * T * cfg.hidden
+
+
 @pytest.mark.parametrize("cfg", small_configs()[:9] + [CONFIGS["tiny"]], ids=lambda c: c.name)
 def test_combine_unweighted_rank_sum(ep, cfg):
     """topk_weights=None: each destination rank's row once (the high-throughput

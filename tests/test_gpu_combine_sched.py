@@ -5,10 +5,13 @@ summed in the same order whichever block claims it.  The counters are zero
 after every launch, so one state serves back-to-back launches on a stream.
 Shapes cover one-token batches (768 tokens over 456 or 608 blocks),
 multi-token batches (many small rows), fewer tokens than blocks, and the
-unweighted rank sum; and two streams combining through one layout at once,
-each with its own counters."""
+unweighted rank sum; and two streams combining through one layout at once
+(the binding gives each stream its own counters).  A launch whose counters
+were not zero, or that shares them with a launch on another stream, reports
+EP_ERRBIT_SCHED."""
 from __future__ import annotations
 
+import ctypes as C
 from dataclasses import replace
 
 import numpy as np
@@ -93,33 +96,102 @@ def test_expert_major_scheduled_combine_equals_static(ep, cfg):
     assert LL.sched.tolist() == [0, 0]
 
 
-def test_overlapping_combines_on_one_layout_with_their_own_counters(ep):
-    """Two streams combine different expert outputs through one layout at the
-    same time, the second with a copy of the layout that has its own
-    counters; each gets exactly its result alone."""
-    cfg = SHAPES[1]
+def _two_outputs(ep, cfg, seed=77):
     c = make_case(cfg)
-    idx, w, x = device_inputs(c)
-    E, R = cfg.num_experts, cfg.num_ranks
-    L = ep.get_dispatch_layout(idx, E, R)
-    L2 = replace(L, sched=ep.alloc_combine_sched(idx.device))
-    rows = ep.worst_case_rows(cfg.num_tokens, cfg.num_topk, R)
+    idx, w, _ = device_inputs(c)
+    L = ep.get_dispatch_layout(idx, cfg.num_experts, cfg.num_ranks)
+    rows = ep.worst_case_rows(cfg.num_tokens, cfg.num_topk, cfg.num_ranks)
     g = torch.Generator(device="cuda")
-    g.manual_seed(77)
+    g.manual_seed(seed)
     ys = [torch.randn((rows, cfg.hidden), device="cuda", generator=g).to(torch.bfloat16)
           for _ in range(2)]
+    return idx, w, L, ys
+
+
+def test_overlapping_combines_through_one_layout_get_their_own_counters(ep):
+    """Two streams combine different expert outputs through one layout at the
+    same time; the binding hands each stream its own counters, so each gets
+    exactly its result alone."""
+    cfg = SHAPES[1]
+    idx, w, L, ys = _two_outputs(ep, cfg)
     alone = [ep.combine(ys[0], idx, w, L), ep.combine(ys[1], idx, w, L)]
     torch.cuda.synchronize()
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     for s in streams:
         s.wait_stream(torch.cuda.current_stream())
     outs = [[], []]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
     for _ in range(3):
-        for i, lay in ((0, L), (1, L2)):  # interleave the two streams' launches
+        for i in (0, 1):  # interleave the two streams' launches
             with torch.cuda.stream(streams[i]):
-                outs[i].append(ep.combine(ys[i], idx, w, lay))
+                outs[i].append(ep.combine(ys[i], idx, w, L, err=err))
     torch.cuda.synchronize()
+    assert int(err.item()) == 0
     for i in (0, 1):
         for o in outs[i]:
             np.testing.assert_array_equal(bits_of(o), bits_of(alone[i]))
-    assert L.sched.tolist() == [0, 0] and L2.sched.tolist() == [0, 0]
+    used = [ep.sched_for(L, idx.device)]
+    for s in streams:
+        with torch.cuda.stream(s):
+            used.append(ep.sched_for(L, idx.device))
+    assert len({t.data_ptr() for t in used}) == 3  # the home stream's and one per side stream
+    assert all(t.tolist() == [0, 0] for t in used)
+
+
+def test_counters_not_zero_at_launch_are_reported(ep):
+    """A claim counter left non-zero (as if another launch had claimed from
+    it) shifts the batches: the launch reports EP_ERRBIT_SCHED, still leaves
+    the counters at zero, and the next launch is exact again."""
+    cfg = SHAPES[1]
+    idx, w, L, ys = _two_outputs(ep, cfg)
+    alone = ep.combine(ys[0], idx, w, L)
+    torch.cuda.synchronize()
+    L.sched[0] = 1
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.combine(ys[0], idx, w, L, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == ep.EP_ERRBIT_SCHED
+    assert L.sched.tolist() == [0, 0]
+    err.zero_()
+    again = ep.combine(ys[0], idx, w, L, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    np.testing.assert_array_equal(bits_of(again), bits_of(alone))
+
+
+def test_shared_counters_on_two_streams_never_go_unreported(ep):
+    """Through the C ABI, two launches on two streams share one counter state
+    (the misuse the binding prevents).  Whenever either output differs from
+    its result alone, the shared error word carries EP_ERRBIT_SCHED.  The
+    persistent grid fills the GPU, so the second launch's blocks start only
+    as the first one's leave, and often after its last block has reset the
+    counters: then both outputs are whole and nothing is reported.  The
+    deterministic case is test_counters_not_zero_at_launch_are_reported."""
+    cfg = Config("sched_overlap", 16, 2048, 4096, 64, 6, routing="zipf", zipf_s=1.2,
+                 mask_prob=0.05, seed=1205)
+    idx, w, L, ys = _two_outputs(ep, cfg)
+    alone = [bits_of(ep.combine(ys[i], idx, w, L)) for i in (0, 1)]
+    lib = ep.lib()
+    sched = ep.alloc_combine_sched(idx.device)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    T, K = idx.shape
+    caught = 0
+    for _ in range(4):
+        sched.zero_()
+        err.zero_()
+        outs = [torch.zeros_like(x[:T]) for x in (ys[0], ys[1])]
+        torch.cuda.synchronize()
+        for i in (0, 1):
+            st = C.c_void_p(streams[i].cuda_stream)
+            status = lib.ep_combine_sched(ys[i].data_ptr(), cfg.hidden, idx.data_ptr(),
+                                          w.data_ptr(), T, K, cfg.num_experts, cfg.num_ranks,
+                                          L.slot.data_ptr(), outs[i].data_ptr(),
+                                          sched.data_ptr(), err.data_ptr(), st)
+            assert status == 0
+        torch.cuda.synchronize()
+        wrong = any(not np.array_equal(bits_of(outs[i]), alone[i]) for i in (0, 1))
+        flagged = bool(int(err.item()) & ep.EP_ERRBIT_SCHED)
+        assert flagged or not wrong, "an incomplete combine went unreported"
+        caught += wrong
+    print(f"{caught} of 4 overlapping pairs lost tokens, all reported")

@@ -7,16 +7,19 @@ fixed at start-up.  For them the layout takes its scratch from a fixed array
 inside the library instead of a caller-provided workspace.  These tests call
 that entry point through the C ABI, twice in a row on different routing (the
 second call reuses the scratch the first one left behind), and require the
-same results as ep_get_dispatch_layout with a workspace.  The layout is
-integer work, so the comparison is bit-exact, as in the other layout tests.
+CPU oracle's layout, and the same results as ep_get_dispatch_layout with a
+workspace.  The layout is integer work, so both comparisons are bit-exact,
+as in the other layout tests.
 """
 from __future__ import annotations
 
 import ctypes as C
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from workloads import CONFIGS, make_case
 
 pytestmark = pytest.mark.gpu
@@ -62,7 +65,14 @@ def _assert_same_layout(a, b):
     assert torch.equal(a.is_token_in_rank.view(torch.uint8), b.is_token_in_rank.view(torch.uint8))
 
 
-def test_noalloc_layout_matches_workspace_layout_on_two_calls_in_a_row(ep):
+def _assert_oracle_layout(got, want):
+    for name in ("num_tokens_per_rank", "num_tokens_per_expert", "slot", "recv_base"):
+        assert np.array_equal(getattr(got, name).cpu().numpy(), getattr(want, name)), name
+    assert np.array_equal(got.is_token_in_rank.view(torch.uint8).cpu().numpy(),
+                          want.is_token_in_rank)
+
+
+def test_noalloc_layout_matches_oracle_on_two_calls_in_a_row(ep):
     big = CONFIGS["skewed"].scaled(2048)   # 32768 tokens, Zipf routing, masked slots
     small = CONFIGS["tiny"]                # 512 tokens, uniform routing
     cases = [make_case(big, with_hidden=False), make_case(small, with_hidden=False)]
@@ -71,11 +81,14 @@ def test_noalloc_layout_matches_workspace_layout_on_two_calls_in_a_row(ep):
            for idx, c in zip(inputs, cases)]  # two calls in a row, no sync between
     torch.cuda.synchronize()
     for (L, err), idx, c in zip(got, inputs, cases):
+        assert int(err.item()) == 0
+        _assert_oracle_layout(L, oracle.layout(c.topk_idx, c.cfg.num_experts, c.cfg.num_ranks))
+        # and the entry point with a caller workspace, on the kernels it picks
         want_err = torch.zeros(1, dtype=torch.int32, device="cuda")
         want = ep.get_dispatch_layout(idx, c.cfg.num_experts, c.cfg.num_ranks, err=want_err)
         torch.cuda.synchronize()
         _assert_same_layout(L, want)
-        assert int(err.item()) == int(want_err.item()) == 0
+        assert int(want_err.item()) == 0
 
 
 def test_noalloc_layout_rejects_problems_beyond_its_scratch(ep):

@@ -148,3 +148,22 @@ def expert_outputs(rows: int, hidden: int, seed: int) -> np.ndarray:
 def random_weights(rng: np.random.Generator, T: int, K: int) -> np.ndarray:
     """Uniform(0,1) float32 weights, for combine cases that need no softmax."""
     return rng.random((T, K)).astype(np.float32)
+
+
+def signed_unit_bf16_bits(rows: int, hidden: int, seed: int) -> np.ndarray:
+    """Stand-in expert outputs for full-size batches, drawn fast: bfloat16 bit
+    patterns with a random sign, exponent 126 or 127 and a random 7-bit
+    mantissa, i.e. values uniform over the bf16 grid of +-[0.5, 2).  One
+    integer draw per element (no float rounding pass), so a few GB of rows
+    take seconds."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = np.empty((rows, hidden), dtype=np.uint16)
+    for r0 in range(0, rows, 16384):
+        r1 = min(rows, r0 + 16384)
+        u = rng.integers(0, 1 << 16, size=(r1 - r0, hidden), dtype=np.uint16)
+        # keep the sign (bit 15), the exponent's lowest bit (bit 7) and the
+        # mantissa (bits 0..6); set exponent bits 8..14 to 0111111 (0x7E/0x7F)
+        np.bitwise_and(u, 0x80FF, out=u)
+        np.bitwise_or(u, 0x3F00, out=u)
+        out[r0:r1] = u
+    return out

@@ -384,6 +384,25 @@ class StepRunner:
         if ev is not None:
             ev[3].record(s)
 
+    def step_isolated(self, ev, flush):
+        """One step with every kernel alone between its own pair of events
+        (ev[0..5]), L2 flushed before each: no kernel is charged for the
+        write-back of the lines the one before it left dirty, nor served
+        from lines it left in L2 (ncu's cache control measures the same)."""
+        s = self.stream
+        flush()
+        ev[0].record(s)
+        self.do_layout()
+        ev[1].record(s)
+        flush()
+        ev[2].record(s)
+        self.do_dispatch(0, self.T)
+        ev[3].record(s)
+        flush()
+        ev[4].record(s)
+        self.do_combine(0, self.T)
+        ev[5].record(s)
+
     def rows(self) -> int:
         if self.args.layout == "ht":
             return self.ep.total_rows(self.L)
@@ -422,18 +441,22 @@ def time_device(run: StepRunner, args, world: int, graph=None, min_region_s: flo
     one's early (programmatic) launch, which costs several microseconds per
     kernel edge.  It is repeated until the passes cover min_region_s (so
     that the clock sampler sees the GPU under load), and the median pass is
-    reported.  One more pass puts an event around every kernel, for the
-    per-kernel durations (layout, dispatch, combine) that the roofline
-    uses; these include that lost overlap.  With an L2 flush (a read of a
-    buffer twice the size of L2, which leaves no dirty lines behind) between
-    steps, a pair of events brackets each step instead and the flush stays
-    outside them."""
+    reported.  With an L2 flush (a read of a buffer twice the size of L2,
+    which leaves no dirty lines behind) between steps, a pair of events
+    brackets each step instead and the flush stays outside them.
+
+    Two more passes of K steps give per-kernel durations.  In the first,
+    each kernel runs alone between its own events with L2 flushed before it
+    (StepRunner.step_isolated): these times feed the roofline.  The second
+    puts an event between the kernels of ordinary steps (in_step): there
+    each kernel also pays for the write-back of the lines the one before it
+    left dirty in L2, and loses its early launch."""
     import torch
     import torch.distributed as dist
     dev, stream, K = run.dev, run.stream, args.steps
     P = run.rows()
     flush = needs_l2_flush(run.cfg, P)
-    scrub = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    scrub = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
 
@@ -472,14 +495,21 @@ def time_device(run: StepRunner, args, world: int, graph=None, min_region_s: flo
         if time.time() - wall0 >= min_region_s or len(passes) >= 200:
             break
     ms_kernels, evs = one_pass(per_kernel=True)
+    iso = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        run.step_isolated(iso[i], lambda: scrub.sum())
+    torch.cuda.synchronize(dev)
     wall1 = time.time()
+    mean = lambda a, b, evl: statistics.mean(e[a].elapsed_time(e[b]) for e in evl)  # noqa: E731
     return {
         "P": P, "flush": flush, "ms": statistics.median(passes), "passes": passes,
         "window": (wall0, wall1),
         "ms_kernels": ms_kernels,
-        "layout_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
-        "dispatch_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
-        "combine_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in evs),
+        "layout_ms": mean(0, 1, iso), "dispatch_ms": mean(2, 3, iso),
+        "combine_ms": mean(4, 5, iso),
+        "in_step": {"layout_ms": mean(0, 1, evs), "dispatch_ms": mean(1, 2, evs),
+                    "combine_ms": mean(2, 3, evs)},
     }
 
 
@@ -652,7 +682,8 @@ def other_workloads(args, ep, dev, peak: float) -> dict:
             "layout_ms": kern["layout"]["ms"], "layout_kernels": kinds,
             "dispatch": {k: kern["dispatch"][k] for k in ("ms", "gbs", "frac")},
             "combine": {k: kern["combine"][k] for k in ("ms", "gbs", "frac")},
-            "kernel_timing_ms_per_step": t["ms_kernels"],
+            "kernel_timing": {"in_step_ms_per_step": t["ms_kernels"],
+                              "in_step": t["in_step"]},
             "recv_rows": P, "dtype": "e4m3+bf16" if cfg.fp8 else "bf16",
             "l2": "flushed between steps (read of 2x L2, outside the per-step events)"
                   if t["flush"] else "inputs larger than L2",
@@ -764,10 +795,15 @@ def run_ours(args, cfg: Config):
             "passes": {"n": len(t["passes"]), "steps_each": args.steps,
                        "ms_min": min(t["passes"]), "ms_max": max(t["passes"]),
                        "note": "value and ms_per_step come from the median pass"},
-            "kernel_timing": {"steps": args.steps, "ms_per_step": ms_with_kernel_events,
-                              "note": "per-kernel events in one more pass of K steps; an event "
-                                      "between two kernels stops the early launch of the second, "
-                                      "so these steps run slower than the plain ones"},
+            "kernel_timing": {"steps": args.steps,
+                              "kernels": "each kernel alone between its own events, with L2 "
+                                         "flushed (a read of twice L2) before it: no kernel pays "
+                                         "for the write-back of the lines the previous one left "
+                                         "dirty",
+                              "in_step": t["in_step"], "in_step_ms_per_step": ms_with_kernel_events,
+                              "note": "in_step: ordinary steps with an event between the kernels; "
+                                      "an event stops the next kernel's early launch, and each "
+                                      "kernel pays for the previous one's dirty lines"},
             "e2e": e2e,
             "gpu_launches": (layout_launches + 2) * args.steps * len(t["passes"]),
             "clocks": clocks,

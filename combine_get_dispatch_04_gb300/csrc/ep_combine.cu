@@ -314,11 +314,10 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
       const int buf = bi & 1;
       const uint32_t use = bi >> 1;
       unsigned long long nxt = 0;  // the next batch, claimed before it is needed
-      if (a.sched && t0 < a.T && lane == 0) {
+      const bool claimed = a.sched && t0 < a.T;
+      if (claimed && lane == 0) {
         nxt = atomicAdd(a.sched, (unsigned long long)claim);
         ++claims;
-        // a launch alone hands out exactly nbatches claims, 0 .. nbatches-1
-        over |= nxt >= (unsigned long long)a.nbatches * (unsigned long long)claim;
       }
       if (use > 0 && !wait_warp(&tempty[buf], (use - 1) & 1, abort)) {
         ok = false;
@@ -334,6 +333,11 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(Args a) {
         tD[e] = gather_token(a, t0 + lane, trows + e * a.dmax, tW + e * a.dmax, bad);
       }
       mbar_arrive(&tfull[buf]);  // every lane releases its own table writes
+      // a launch alone hands out exactly nbatches claims, 0 .. nbatches-1.
+      // Checked only here, so that the claim's round trip (all blocks claim
+      // at once at the start) overlaps the gather instead of delaying it.
+      if (claimed && lane == 0)
+        over |= nxt >= (unsigned long long)a.nbatches * (unsigned long long)claim;
       if (n == 0) break;
       t0 = a.sched ? dyn0 + (int64_t)__shfl_sync(0xFFFFFFFFu, nxt, 0) : t0 + dyn0;
     }

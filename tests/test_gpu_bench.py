@@ -48,11 +48,12 @@ def test_bench_line_on_the_small_workload(ep, layout, graph):
     assert d["gpu_launches"] == 3 * d["steps"] * d["passes"]["n"]
     assert "workloads" not in d  # only the default run carries the other workloads
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
-    # the per-kernel times come from a second pass of the same number of steps
+    # per-kernel times: each kernel alone (roofline), and inside ordinary steps
     kt = d["kernel_timing"]
-    assert kt["steps"] == 5 and kt["ms_per_step"] > 0
-    parts = sum(d["kernels"][k]["ms"] for k in ("layout", "dispatch", "combine"))
-    assert parts == pytest.approx(kt["ms_per_step"], rel=0.02)
+    assert kt["steps"] == 5 and kt["in_step_ms_per_step"] > 0
+    parts = sum(kt["in_step"][k + "_ms"] for k in ("layout", "dispatch", "combine"))
+    assert parts == pytest.approx(kt["in_step_ms_per_step"], rel=0.02)
+    assert all(d["kernels"][k]["ms"] > 0 for k in ("layout", "dispatch", "combine"))
     assert (d["config"].get("step_launch") == "cuda_graph_replay") == graph
     if layout == "ht":
         cb = d["cpu_baseline"]

@@ -44,6 +44,7 @@ UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 << 20  # GB300 L2
 DEFAULT_CONFIG = "skewed"  # the largest bf16 workload (most bytes moved per phase)
+FUSED_AUTO_MAX_TOKENS = 0  # largest batch the default step runs as one fused launch
 
 
 # ----------------------------------------------------------------------------
@@ -303,6 +304,12 @@ class StepRunner:
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.stream = torch.cuda.current_stream(dev)
         self.views = {}  # (a, b) -> the layout's rows of those tokens, made once
+        # layout and dispatch in one launch (small batches)
+        self.fused = args.layout == "ht" and (
+            args.layout_kernels == "fused" or
+            (args.layout_kernels == "auto" and auto_fused(ep, cfg)))
+        if args.layout_kernels == "fused" and not ep.fused_fits(T, R, E):
+            raise SystemExit("--layout-kernels fused: the batch does not fit the one-launch form")
         if args.layout == "ht":
             # rank-major: worst-case capacity T * min(K, R) rows, no host sync per step
             self.cap = ep.worst_case_rows(T, K, R)
@@ -346,11 +353,22 @@ class StepRunner:
     def do_layout(self):
         ep, cfg = self.ep, self.cfg
         if self.args.layout == "ht":
+            path = "auto" if self.args.layout_kernels == "fused" else self.args.layout_kernels
             ep.get_dispatch_layout(self.idx, cfg.num_experts, cfg.num_ranks, err=self.err,
-                                   out=self.L, path=self.args.layout_kernels)
+                                   out=self.L, path=path)
         else:
             ep.ll_get_dispatch_layout(self.idx, cfg.num_experts, cfg.num_ranks, err=self.err,
                                       out=self.L, path=self.args.layout_kernels)
+
+    def do_layout_dispatch(self):
+        """The step's layout and dispatch: one fused launch, or the two calls."""
+        if self.fused:
+            self.ep.layout_dispatch(self.x, self.idx, self.w, self.cfg.num_experts,
+                                    self.cfg.num_ranks, use_fp8=self.cfg.fp8, err=self.err,
+                                    layout=self.L, out=self.D)
+        else:
+            self.do_layout()
+            self.do_dispatch(0, self.T)
 
     def do_dispatch(self, a, b):
         Lc = self._view(a, b)
@@ -374,10 +392,15 @@ class StepRunner:
         s = self.stream
         if ev is not None:
             ev[0].record(s)
-        self.do_layout()
-        if ev is not None and per_kernel:
-            ev[1].record(s)
-        self.do_dispatch(0, self.T)
+        if self.fused:  # layout + dispatch in one launch: the layout's share reads 0
+            if ev is not None and per_kernel:
+                ev[1].record(s)
+            self.do_layout_dispatch()
+        else:
+            self.do_layout()
+            if ev is not None and per_kernel:
+                ev[1].record(s)
+            self.do_dispatch(0, self.T)
         if ev is not None and per_kernel:
             ev[2].record(s)
         self.do_combine(0, self.T)
@@ -392,11 +415,15 @@ class StepRunner:
         s = self.stream
         flush()
         ev[0].record(s)
-        self.do_layout()
+        if not self.fused:
+            self.do_layout()
         ev[1].record(s)
         flush()
         ev[2].record(s)
-        self.do_dispatch(0, self.T)
+        if self.fused:
+            self.do_layout_dispatch()
+        else:
+            self.do_dispatch(0, self.T)
         ev[3].record(s)
         flush()
         ev[4].record(s)
@@ -410,6 +437,8 @@ class StepRunner:
 
     def layout_launches(self):
         ep, args, cfg = self.ep, self.args, self.cfg
+        if self.fused:
+            return 0, "fused"  # counted with the dispatch's launch
         T, K, R, E = cfg.num_tokens, cfg.num_topk, cfg.num_ranks, cfg.num_experts
         if args.layout == "ll":
             if args.layout_kernels == "single" or (args.layout_kernels == "auto"
@@ -422,6 +451,13 @@ class StepRunner:
         # count + assign, with the scan folded in unless R * blocks > 8192 (T > 0)
         nb = R * ((T // R + 511) // 512)
         return (2 if R * nb <= 8192 else 3), "multi"
+
+
+def auto_fused(ep, cfg: Config) -> bool:
+    """The default step fuses layout and dispatch into one launch for the
+    batches where that measured faster (decode-size batches)."""
+    return ep.fused_fits(cfg.num_tokens, cfg.num_ranks, cfg.num_experts) and \
+        cfg.num_tokens <= FUSED_AUTO_MAX_TOKENS
 
 
 def needs_l2_flush(cfg: Config, P: int) -> bool:
@@ -830,9 +866,11 @@ def main(argv=None):
                     help="scale the workload (same recipe) for profiling runs")
     ap.add_argument("--layout", choices=["ht", "ll"], default="ht",
                     help="receive layout: rank-major (ht, default) or expert-major (ll)")
-    ap.add_argument("--layout-kernels", choices=["auto", "multi", "single"], default="auto",
+    ap.add_argument("--layout-kernels", choices=["auto", "multi", "single", "fused"],
+                    default="auto",
                     help="layout kernels: one cluster launch (single, small batches), the "
-                         "multi-launch form, or the library's choice (auto)")
+                         "multi-launch form, layout and dispatch in one launch (fused, small "
+                         "batches), or the benchmark's choice (auto)")
     ap.add_argument("--graph", action="store_true",
                     help="time the plain steps as replays of one CUDA graph of the step "
                          "(no host launch cost; the per-kernel pass stays eager)")

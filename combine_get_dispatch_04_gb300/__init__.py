@@ -43,10 +43,14 @@ EXPORTED = ("ep_status_string", "ep_workspace_bytes", "ep_get_dispatch_layout",
             "ep_combine", "ep_ll_workspace_bytes", "ep_ll_get_dispatch_layout",
             "ep_ll_dispatch", "ep_ll_combine", "ep_debug_set_combine_stall",
             "ep_ll_layout_single_launch_fits", "ep_ll_layout_auto_single_launch",
-            "ep_ll_get_dispatch_layout_path", "ep_combine_sched", "ep_ll_combine_sched")
+            "ep_ll_get_dispatch_layout_path", "ep_combine_sched", "ep_ll_combine_sched",
+            "ep_layout_dispatch_fused_fits", "ep_layout_dispatch_fused",
+            "ep_layout_dispatch_fused_workspace_bytes", "ep_debug_set_fused_stall")
 
 # 64-bit words of a combine's scheduling counters (EP_COMBINE_SCHED_WORDS)
 COMBINE_SCHED_WORDS = 2
+# 64-bit words of the fused layout + dispatch's counters (EP_FUSED_SYNC_WORDS)
+FUSED_SYNC_WORDS = 640
 
 _lib = None
 
@@ -95,10 +99,19 @@ def load(path: str | None = None) -> C.CDLL:
     L.ep_ll_combine.argtypes = [P, i32, P, i64, i32, P, P, P, P]
     L.ep_combine_sched.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, P, P, P]
     L.ep_ll_combine_sched.argtypes = [P, i32, P, i64, i32, P, P, P, P, P]
+    L.ep_layout_dispatch_fused_fits.argtypes = [i64, i32, i32]
+    L.ep_layout_dispatch_fused_fits.restype = i32
+    L.ep_layout_dispatch_fused_workspace_bytes.argtypes = [i64, i32, i32]
+    L.ep_layout_dispatch_fused_workspace_bytes.restype = sz
+    L.ep_layout_dispatch_fused.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, P, P, P, i64,
+                                           i32, P, P, P, P, P, P, P, sz, P, P, P]
+    L.ep_debug_set_fused_stall.argtypes = [i32]
+    L.ep_debug_set_fused_stall.restype = None
     for name in ("ep_get_dispatch_layout", "ep_get_dispatch_layout_path",
                  "ep_layout_total_rows", "ep_dispatch", "ep_combine",
                  "ep_ll_get_dispatch_layout", "ep_ll_get_dispatch_layout_path",
-                 "ep_ll_dispatch", "ep_ll_combine", "ep_combine_sched", "ep_ll_combine_sched"):
+                 "ep_ll_dispatch", "ep_ll_combine", "ep_combine_sched", "ep_ll_combine_sched",
+                 "ep_layout_dispatch_fused"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -182,6 +195,9 @@ class Layout:
     # of their own (sched_for), so that combines through one Layout on two
     # streams, or a graph replayed beside eager calls, never share them.
     sched: torch.Tensor | None = None
+    # [FUSED_SYNC_WORDS] int64 counters and flags of the one-launch layout +
+    # dispatch, zero between launches; per stream like sched
+    fused_sync: torch.Tensor | None = None
 
     @property
     def num_tokens(self) -> int:
@@ -214,11 +230,15 @@ def alloc_layout(num_tokens: int, num_experts: int, num_ranks: int,
     so that the same Layout serves either path)."""
     T, R, E = num_tokens, num_ranks, num_experts
     i32 = dict(dtype=torch.int32, device=device)
-    ws = torch.empty(max(workspace_bytes(T, R, E), 16), dtype=torch.uint8, device=device)
+    # one workspace for the multi-launch layout and the one-launch layout + dispatch
+    wsb = max(workspace_bytes(T, R, E),
+              int(lib().ep_layout_dispatch_fused_workspace_bytes(T, R, E)), 16)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=device)
     return Layout(torch.empty((R, R), **i32), torch.empty((R, E), **i32),
                   torch.empty((T, R), dtype=torch.bool, device=device),
                   torch.empty((T, R), **i32), torch.empty(R + 1, **i32), E, R, ws,
-                  alloc_combine_sched(device))
+                  alloc_combine_sched(device),
+                  torch.zeros(FUSED_SYNC_WORDS, dtype=torch.int64, device=device))
 
 
 def get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int, *,
@@ -320,18 +340,13 @@ def dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor
     return out
 
 
-def sched_for(layout, device: torch.device) -> torch.Tensor | None:
-    """The scheduling counters that a combine through `layout` on the current
-    stream uses.  The layout's own counters belong to the first stream that
-    uses them (recorded on the tensor, so copies of the Layout agree); a
-    combine on any other stream gets counters kept for that stream, zeroed
-    when first needed.  None: the layout asks for the static schedule."""
-    s = layout.sched
-    if s is None:
-        return None
-    _need(s, "sched", torch.int64, (COMBINE_SCHED_WORDS,))
+def _per_stream(s: torch.Tensor, name: str, words: int, device: torch.device) -> torch.Tensor:
+    """Counter state `s` serves the first stream that uses it (recorded on
+    the tensor, so copies of a Layout agree); any other stream gets a state
+    of its own, kept on `s` and zeroed when first needed."""
+    _need(s, name, torch.int64, (words,))
     if s.device != device:
-        raise EPError("the layout's sched must be on the combine's device")
+        raise EPError(f"the layout's {name} must be on the call's device")
     key = torch.cuda.current_stream(device).cuda_stream
     home = getattr(s, "_ep_home_stream", None)
     if home is None:
@@ -340,8 +355,60 @@ def sched_for(layout, device: torch.device) -> torch.Tensor | None:
         return s
     others = s.__dict__.setdefault("_ep_other_streams", {})
     if key not in others:
-        others[key] = alloc_combine_sched(device)
+        others[key] = torch.zeros(words, dtype=torch.int64, device=device)
     return others[key]
+
+
+def sched_for(layout, device: torch.device) -> torch.Tensor | None:
+    """The scheduling counters that a combine through `layout` on the current
+    stream uses (see _per_stream).  None: the layout asks for the static
+    schedule."""
+    s = layout.sched
+    return None if s is None else _per_stream(s, "sched", COMBINE_SCHED_WORDS, device)
+
+
+def fused_fits(num_tokens: int, num_ranks: int, num_experts: int) -> bool:
+    """True if layout_dispatch (one launch) applies to the batch."""
+    return bool(lib().ep_layout_dispatch_fused_fits(num_tokens, num_ranks, num_experts))
+
+
+def layout_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor,
+                    num_experts: int, num_ranks: int, *, use_fp8: bool = False,
+                    capacity: int | None = None, err: torch.Tensor | None = None,
+                    layout: Layout | None = None,
+                    out: Dispatched | None = None) -> tuple[Layout, Dispatched]:
+    """get_dispatch_layout and dispatch in one kernel launch (small batches:
+    fused_fits).  Same outputs as the two calls.  Enqueued on the current
+    stream."""
+    _need(x, "x", torch.bfloat16)
+    T, H = x.shape
+    _need(topk_idx, "topk_idx", torch.int64)
+    K = topk_idx.shape[1]
+    _need(topk_idx, "topk_idx", torch.int64, (T, K))
+    _need(topk_weights, "topk_weights", torch.float32, (T, K))
+    R, E = num_ranks, num_experts
+    L = layout if layout is not None else alloc_layout(T, E, R, x.device)
+    _need(L.slot, "slot", torch.int32, (T, R))
+    if L.fused_sync is None:
+        raise EPError("the layout has no fused_sync state")
+    sync = _per_stream(L.fused_sync, "fused_sync", FUSED_SYNC_WORDS, x.device)
+    if out is None:
+        cap = capacity if capacity is not None else worst_case_rows(T, K, R)
+        out = alloc_dispatched(cap, H, K, E, R, use_fp8, x.device)
+    elif out.use_fp8 != use_fp8:
+        raise EPError("preallocated dispatch buffers have the wrong payload type")
+    if err is not None:
+        _need(err, "err", torch.int32)
+    _check(lib().ep_layout_dispatch_fused(
+        _ptr(x), H, _ptr(topk_idx), _ptr(topk_weights), T, K, E, R,
+        _ptr(L.num_tokens_per_rank), _ptr(L.num_tokens_per_expert), _ptr(L.is_token_in_rank),
+        _ptr(L.slot), _ptr(L.recv_base), out.recv_x.shape[0], int(use_fp8), _ptr(out.recv_x),
+        _ptr(out.recv_scales), _ptr(out.recv_src_idx), _ptr(out.recv_topk_idx),
+        _ptr(out.recv_topk_weights), _ptr(out.num_recv_tokens_per_expert), _ptr(L.workspace),
+        L.workspace.numel(), _ptr(sync), _ptr(err), _stream(x.device)),
+        "ep_layout_dispatch_fused")
+    _debug_check("layout_dispatch", err, x.device)
+    return L, out
 
 
 def combine(y: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor | None,

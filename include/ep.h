@@ -274,6 +274,69 @@ ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk_idx,
                        int32_t* err_word, ep_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Layout and dispatch in one launch, for small (decode-size) batches.
+ *
+ * The same outputs as ep_get_dispatch_layout followed by ep_dispatch, from
+ * one kernel launch: the pages run layout, the count exchange that fixes
+ * the receive offsets (notify_dispatch, cached_notify: "[Not ready] MSCCLPP
+ * EP implementation", section "Scope", Internode HT) and the data movement
+ * as separate kernels; on one GPU the exchange becomes a wait inside one
+ * grid.  The first blocks of the grid to start (picked by an atomic ticket,
+ * so that no block waits on one that has not started) compute the layout
+ * and meet at a bounded barrier; every block loads its share of x at once
+ * and waits, bounded, for the layout before it scatters.  At these sizes the
+ * layout is bound by latency, and the fused launch hides the x loads behind
+ * it and saves the launches between the kernels.
+ *
+ * Fits (ep_layout_dispatch_fused_fits): 1 <= T <= 16384 and at most 8192
+ * ballots, R * R * ceil(T_r / 32) <= 8192 (one 32-bit ballot per
+ * destination and group of 32 tokens, groups never straddling two source
+ * ranks): the 4096-token decode batch at 32 ranks, or 16384 tokens at 8
+ * ranks.  Other sizes return EP_ERR_INVALID_ARG with nothing enqueued.
+ * Arguments: those of ep_get_dispatch_layout (its outputs, all required)
+ *   and of ep_dispatch (slot is written here and read back by the scatter;
+ *   num_recv_tokens_per_expert is computed here, nullable), plus:
+ * workspace (device): ep_layout_dispatch_fused_workspace_bytes(T, R, E)
+ *   bytes (about 8 * R * R * ceil(T_r / 32)); EP_ERR_CAPACITY if smaller.
+ *   No initialisation needed.
+ * sync (device, EP_FUSED_SYNC_WORDS 64-bit words, 8-byte aligned): the
+ *   grid's counters (start ticket, barrier, layout done, blocks left) and
+ *   release flags, spread over 256-byte lines.  The caller zeroes them once;
+ *   every launch leaves them zero again when its last block exits,
+ *   including a launch whose waits ran out.  Launches that can overlap on
+ *   the GPU need separate states.
+ * err_word: as ep_get_dispatch_layout and ep_dispatch, plus
+ *   EP_ERRBIT_TIMEOUT if a bounded wait (1 s) ran out: the layout or its
+ *   barrier did not complete, and no row was dispatched.
+ * ------------------------------------------------------------------------ */
+#define EP_FUSED_SYNC_WORDS 640
+
+/* 1 if (T, R, E) fits the one-launch layout + dispatch, else 0. */
+int ep_layout_dispatch_fused_fits(int64_t num_tokens, int num_ranks, int num_experts);
+
+/* Bytes of workspace ep_layout_dispatch_fused needs (0 if it does not fit). */
+size_t ep_layout_dispatch_fused_workspace_bytes(int64_t num_tokens, int num_ranks,
+                                                int num_experts);
+
+ep_status_t ep_layout_dispatch_fused(
+    const void* x, int hidden, const int64_t* topk_idx, const float* topk_weights,
+    int64_t num_tokens, int num_topk, int num_experts, int num_ranks,
+    int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+    int32_t* slot, int32_t* recv_base, int64_t recv_capacity_rows, int use_fp8, void* recv_x,
+    float* recv_scales, int32_t* recv_src_idx, int64_t* recv_topk_idx, float* recv_topk_weights,
+    int32_t* num_recv_tokens_per_expert, void* workspace, size_t workspace_bytes,
+    uint64_t* sync, int32_t* err_word, ep_stream_t stream);
+
+/*
+ * Test hook for the bounded waits of ep_layout_dispatch_fused: the next
+ * launch from this host thread leaves the first layout block's barrier
+ * arrival out, so the barrier and the wait for the layout run out after
+ * about 1 s each; the launch then reports EP_ERRBIT_TIMEOUT, dispatches
+ * nothing, and still returns its state to zero.  One-shot; 0 cancels it.
+ */
+void ep_debug_set_fused_stall(int on);
+
+/* ------------------------------------------------------------------------
  * Low-latency (expert-major) layout: the receive layout of the low-latency
  * kernels ("[Not ready] MSCCLPP EP implementation", the low-latency port:
  * dispatch<kUseFP8,...> and combine over per-expert buffers indexed

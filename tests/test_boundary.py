@@ -216,3 +216,34 @@ def test_error_word_description():
     assert "expert id" in ep.describe_error_word(ep.EP_ERRBIT_BAD_EXPERT)
     both = ep.describe_error_word(ep.EP_ERRBIT_CAPACITY | ep.EP_ERRBIT_TIMEOUT)
     assert "capacity" in both and "wait" in both
+
+
+def test_fused_fits_and_rejects_bad_arguments(eplib):
+    fits = eplib.ep_layout_dispatch_fused_fits
+    assert fits(4096, 32, 256) == 1          # the decode workload
+    assert fits(512, 4, 16) == 1
+    assert fits(16384, 8, 256) == 1           # 8 * 8 * 64 = 4096 ballots
+    assert fits(16384 + 8, 8, 256) == 0       # above the token limit
+    assert fits(0, 4, 16) == 0                # empty batches take the separate calls
+    assert fits(8192, 32, 256) == 1           # 32 * 32 * 8 = 8192 ballots
+    assert fits(8192 + 32 * 32, 32, 256) == 0  # 32 * 32 * 9 ballots
+    assert fits(4096, 64, 128) == 1           # 64 * 64 * 2 ballots
+    assert fits(10, 4, 16) == 0               # T % R
+    f = eplib.ep_layout_dispatch_fused
+    p = C.c_void_p(4096)  # never dereferenced: the checks fail first
+    bad_sync = C.c_void_p(4100)
+
+    def call(T=512, K=4, E=16, R=4, H=256, fp8=0, sync=p, ws_bytes=1 << 20):
+        return f(p, H, p, p, T, K, E, R, p, p, p, p, p, T * 4, fp8, p, p, None, None, None, None,
+                 p, ws_bytes, sync, None, None)
+
+    assert call(T=16392, R=8, E=256) == EP_ERR_INVALID_ARG
+    assert call(H=12) == EP_ERR_INVALID_ARG
+    assert call(H=256 + 8, fp8=1) == EP_ERR_INVALID_ARG   # FP8 needs H % 128
+    assert call(sync=None) == EP_ERR_INVALID_ARG
+    assert call(sync=bad_sync) == EP_ERR_INVALID_ARG      # 8-byte alignment
+    need = eplib.ep_layout_dispatch_fused_workspace_bytes(512, 4, 16)
+    # ballots then offsets, R * R * ceil(T_r / 32) of each, the ballots padded to 256 bytes
+    assert need == 256 + 4 * 4 * 4 * 4
+    assert eplib.ep_layout_dispatch_fused_workspace_bytes(16392, 8, 256) == 0
+    assert call(ws_bytes=need - 1) == EP_ERR_CAPACITY

@@ -27,6 +27,7 @@ def lib():
         i64, i32 = C.c_int64, C.c_int
         L.oracle_layout.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P, P]
         L.oracle_num_recv_tokens_per_expert.argtypes = [P, i32, i32, P]
+        L.oracle_shard_layout.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P, P]
         L.oracle_dispatch.argtypes = [P, i64, i64, P, P, i32, i32, i32, P, i64, i64, i32,
                                       P, P, P, P, P]
         L.oracle_combine.argtypes = [P, i64, P, P, i64, i32, i32, i32, P, i64, i64, P]
@@ -40,7 +41,7 @@ def lib():
                      "oracle_bf16_to_double_n", "oracle_e4m3_to_double_n"):
             getattr(L, name).argtypes = [P, i64, P]
             getattr(L, name).restype = None
-        for name in ("oracle_layout", "oracle_num_recv_tokens_per_expert",
+        for name in ("oracle_layout", "oracle_num_recv_tokens_per_expert", "oracle_shard_layout",
                      "oracle_dispatch", "oracle_combine", "oracle_combine_ranksum",
                      "oracle_ll_layout", "oracle_ll_dispatch", "oracle_ll_combine"):
             getattr(L, name).restype = C.c_int
@@ -87,6 +88,32 @@ def layout(topk_idx: np.ndarray, num_experts: int, num_ranks: int) -> Layout:
     _check(lib().oracle_layout(_p(topk_idx), T, K, E, R, _p(itr), _p(ntpr), _p(ntpe),
                                _p(slot), _p(base), _p(err)), "layout")
     return Layout(itr, ntpr, ntpe, slot, base, int(err[0]))
+
+
+@dataclass
+class ShardLayout:
+    is_token_in_rank: np.ndarray  # [T, R] uint8
+    send_counts: np.ndarray       # [R] int32
+    expert_counts: np.ndarray     # [E] int32
+    send_slot: np.ndarray         # [T, R] int32, -1 = not sent
+    send_base: np.ndarray         # [R + 1] int32
+    err_bits: int
+
+
+def shard_layout(topk_idx: np.ndarray, num_experts: int, num_ranks: int) -> ShardLayout:
+    """One rank's layout of its own tokens over num_ranks destinations."""
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    T, K = topk_idx.shape
+    R, E = num_ranks, num_experts
+    itr = np.empty((T, R), np.uint8)
+    cnt = np.empty(R, np.int32)
+    ecnt = np.empty(E, np.int32)
+    slot = np.empty((T, R), np.int32)
+    base = np.empty(R + 1, np.int32)
+    err = np.zeros(1, np.int32)
+    _check(lib().oracle_shard_layout(_p(topk_idx), T, K, E, R, _p(itr), _p(cnt), _p(ecnt),
+                                     _p(slot), _p(base), _p(err)), "shard_layout")
+    return ShardLayout(itr, cnt, ecnt, slot, base, int(err[0]))
 
 
 def num_recv_tokens_per_expert(num_tokens_per_expert: np.ndarray, num_experts: int,

@@ -217,6 +217,59 @@ int oracle_layout(const int64_t* topk_idx, int64_t T, int K, int E, int R,
   return ORACLE_OK;
 }
 
+/*
+ * The sharded form: one rank's layout of its own T tokens over R
+ * destination ranks ("Scope", Intranode: get_dispatch_layout runs on every
+ * rank over its own tokens).  With one source, the definitions above become
+ *   is_token_in_rank[t][r] as above
+ *   send_counts[r]         = sum over t of is_token_in_rank[t][r]
+ *   expert_counts[e]       = number of slots (t,k) with topk_idx[t][k] == e
+ *   send_base[r]           = exclusive prefix of send_counts; send_base[R]
+ *                            = rows of the send buffer
+ *   send_slot[t][r]        = send_base[r] + #{t' < t in rank r}
+ *                            if is_token_in_rank[t][r], else -1
+ * (any T >= 0).  Reading: the send buffer is packed destination-major in
+ * token order, so destination r's rows are one contiguous run; the receiver
+ * stores the runs in source-rank order, which is the slot order above.
+ */
+int oracle_shard_layout(const int64_t* topk_idx, int64_t T, int K, int E, int R,
+                        uint8_t* is_token_in_rank, int32_t* send_counts,
+                        int32_t* expert_counts, int32_t* send_slot, int32_t* send_base,
+                        int32_t* err_bits) {
+  if (T < 0 || K < 1 || E < 1 || R < 1 || E % R) return ORACLE_BAD_ARG;
+  const int El = E / R;
+  *err_bits = 0;
+  memset(send_counts, 0, sizeof(int32_t) * (size_t)R);
+  memset(expert_counts, 0, sizeof(int32_t) * (size_t)E);
+  memset(is_token_in_rank, 0, (size_t)T * R);
+  for (int64_t t = 0; t < T; ++t) {
+    for (int k = 0; k < K; ++k) {
+      int64_t e = topk_idx[t * K + k];
+      if (e == -1) continue;
+      if (e < -1 || e >= E) {
+        *err_bits |= ORACLE_ERR_BAD_EXPERT;
+        continue;
+      }
+      is_token_in_rank[t * R + e / El] = 1;
+      expert_counts[e] += 1;
+    }
+  }
+  for (int64_t t = 0; t < T; ++t)
+    for (int r = 0; r < R; ++r) send_counts[r] += is_token_in_rank[t * R + r];
+  send_base[0] = 0;
+  for (int r = 0; r < R; ++r) send_base[r + 1] = send_base[r] + send_counts[r];
+  for (int r = 0; r < R; ++r) {
+    int32_t seen = 0;
+    for (int64_t t = 0; t < T; ++t) {
+      if (is_token_in_rank[t * R + r])
+        send_slot[t * R + r] = send_base[r] + seen++;
+      else
+        send_slot[t * R + r] = -1;
+    }
+  }
+  return ORACLE_OK;
+}
+
 /* num_recv_tokens_per_expert[r][j]: slots that destination rank r receives
    for its local expert j, summed over source ranks. */
 int oracle_num_recv_tokens_per_expert(const int32_t* num_tokens_per_expert, int E, int R,

@@ -658,3 +658,75 @@ def test_ll_round_trip_identity_experts():
     w = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
     out = oracle.ll_combine(recv, w, L.ll_slot)
     assert np.array_equal(oracle.bf16_to_double(out), oracle.bf16_to_double(c.x_bits))
+
+
+# ---------------------------------------------------------------------------
+# sharded form: one rank's layout of its own tokens (oracle.shard_layout)
+# ---------------------------------------------------------------------------
+def brute_shard_layout(topk_idx, E, R):
+    """Each destination's send run built directly: walk the destinations in
+    order and, within each, the tokens in order."""
+    T, K = topk_idx.shape
+    El = E // R
+    members = [set() for _ in range(T)]
+    per_expert = [0] * E
+    bad = 0
+    for t in range(T):
+        for k in range(K):
+            e = int(topk_idx[t, k])
+            if e == -1:
+                continue
+            if not (0 <= e < E):
+                bad = 1
+                continue
+            members[t].add(e // El)
+            per_expert[e] += 1
+    slot = np.full((T, R), -1, np.int32)
+    base = [0]
+    row = 0
+    for r in range(R):
+        for t in range(T):
+            if r in members[t]:
+                slot[t, r] = row
+                row += 1
+        base.append(row)
+    return dict(slot=slot, base=np.array(base, np.int32),
+                counts=np.diff(np.array(base, np.int32)),
+                per_expert=np.array(per_expert, np.int32), bad=bad)
+
+
+@pytest.mark.parametrize("T,R,E,K,seed", [(0, 4, 16, 4, 1), (1, 1, 3, 2, 2), (7, 3, 6, 2, 3),
+                                          (33, 5, 10, 3, 4), (64, 8, 64, 8, 5),
+                                          (13, 64, 128, 8, 6), (200, 4, 16, 4, 7)])
+def test_shard_layout_matches_brute_force(T, R, E, K, seed):
+    rng = np.random.default_rng(seed)
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int64)
+    idx[rng.random((T, K)) < 0.15] = -1
+    if T > 3:
+        idx[2, 0] = E + 5  # a bad id: treated as masked and flagged
+        idx[3, K - 1] = idx[3, 0]  # a duplicate expert: membership is an OR, counts count slots
+    got = oracle.shard_layout(idx, E, R)
+    want = brute_shard_layout(idx, E, R)
+    np.testing.assert_array_equal(got.send_slot, want["slot"])
+    np.testing.assert_array_equal(got.send_base, want["base"])
+    np.testing.assert_array_equal(got.send_counts, want["counts"])
+    np.testing.assert_array_equal(got.expert_counts, want["per_expert"])
+    assert got.err_bits == want["bad"]
+    # send_slot is a bijection onto [0, rows)
+    live = got.send_slot[got.send_slot >= 0]
+    np.testing.assert_array_equal(np.sort(live), np.arange(got.send_base[-1]))
+
+
+def test_shard_layout_rows_are_the_single_call_rows_of_one_source():
+    """With the whole batch as one rank's tokens (T % R == 0), the send slots
+    are the single-call layout's slots and the counts its column sums: the
+    slot order within a destination is token order either way."""
+    cfg = CONFIGS["skewed"].scaled(64)
+    c = make_case(cfg, with_hidden=False)
+    E, R = cfg.num_experts, cfg.num_ranks
+    sh = oracle.shard_layout(c.topk_idx, E, R)
+    full = oracle.layout(c.topk_idx, E, R)
+    np.testing.assert_array_equal(sh.send_slot, full.slot)
+    np.testing.assert_array_equal(sh.send_base, full.recv_base)
+    np.testing.assert_array_equal(sh.send_counts, full.num_tokens_per_rank.sum(axis=0))
+    np.testing.assert_array_equal(sh.expert_counts, full.num_tokens_per_expert.sum(axis=0))

@@ -18,6 +18,7 @@ import ctypes as C
 import os
 from dataclasses import dataclass
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -45,7 +46,9 @@ EXPORTED = ("ep_status_string", "ep_workspace_bytes", "ep_get_dispatch_layout",
             "ep_ll_layout_single_launch_fits", "ep_ll_layout_auto_single_launch",
             "ep_ll_get_dispatch_layout_path", "ep_combine_sched", "ep_ll_combine_sched",
             "ep_layout_dispatch_fused_fits", "ep_layout_dispatch_fused",
-            "ep_layout_dispatch_fused_workspace_bytes", "ep_debug_set_fused_stall")
+            "ep_layout_dispatch_fused_workspace_bytes", "ep_debug_set_fused_stall",
+            "ep_shard_workspace_bytes", "ep_shard_layout", "ep_shard_offsets",
+            "ep_shard_recv_tokens_per_expert")
 
 # 64-bit words of a combine's scheduling counters (EP_COMBINE_SCHED_WORDS)
 COMBINE_SCHED_WORDS = 2
@@ -107,11 +110,17 @@ def load(path: str | None = None) -> C.CDLL:
                                            i32, P, P, P, P, P, P, P, sz, P, P, P]
     L.ep_debug_set_fused_stall.argtypes = [i32]
     L.ep_debug_set_fused_stall.restype = None
+    L.ep_shard_workspace_bytes.argtypes = [i64, i32, i32]
+    L.ep_shard_workspace_bytes.restype = sz
+    L.ep_shard_layout.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
+    L.ep_shard_offsets.argtypes = [P, i32, i32, P, P]
+    L.ep_shard_recv_tokens_per_expert.argtypes = [P, i32, i32, i32, P]
     for name in ("ep_get_dispatch_layout", "ep_get_dispatch_layout_path",
                  "ep_layout_total_rows", "ep_dispatch", "ep_combine",
                  "ep_ll_get_dispatch_layout", "ep_ll_get_dispatch_layout_path",
                  "ep_ll_dispatch", "ep_ll_combine", "ep_combine_sched", "ep_ll_combine_sched",
-                 "ep_layout_dispatch_fused"):
+                 "ep_layout_dispatch_fused", "ep_shard_layout", "ep_shard_offsets",
+                 "ep_shard_recv_tokens_per_expert"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -330,11 +339,14 @@ def dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor
     cap = out.recv_x.shape[0]
     if err is not None:
         _need(err, "err", torch.int32)
+    # a shard's layout has no [R, E] per-source counts: no per-expert receive counts here
+    ntpe = getattr(layout, "num_tokens_per_expert", None)
+    nrpe = out.num_recv_tokens_per_expert if ntpe is not None else None
     _check(lib().ep_dispatch(
         _ptr(x), H, _ptr(topk_idx), _ptr(topk_weights), T, K, E, R, _ptr(layout.slot),
-        _ptr(layout.num_tokens_per_expert), cap, int(use_fp8), _ptr(out.recv_x),
+        _ptr(ntpe), cap, int(use_fp8), _ptr(out.recv_x),
         _ptr(out.recv_scales), _ptr(out.recv_src_idx), _ptr(out.recv_topk_idx),
-        _ptr(out.recv_topk_weights), _ptr(out.num_recv_tokens_per_expert), _ptr(err),
+        _ptr(out.recv_topk_weights), _ptr(nrpe), _ptr(err),
         _stream(x.device)), "ep_dispatch")
     _debug_check("dispatch", err, x.device)
     return out
@@ -435,6 +447,87 @@ def combine(y: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor 
                                   _ptr(layout.slot), _ptr(out), _ptr(sched), _ptr(err),
                                   _stream(y.device)), "ep_combine_sched")
     _debug_check("combine", err, y.device)
+    return out
+
+
+# --------------------------------------------------------------------------
+# sharded form: one rank's own tokens (the exchange is in .sharded)
+# --------------------------------------------------------------------------
+@dataclass
+class ShardLayout:
+    """Outputs of shard_layout (all on the device)."""
+    send_counts: torch.Tensor       # [R] int32: tokens sent to each destination rank
+    expert_counts: torch.Tensor     # [E] int32: slots naming each expert
+    is_token_in_rank: torch.Tensor  # [T, R] bool
+    send_slot: torch.Tensor         # [T, R] int32: row in the send buffer, -1 = not sent
+    send_base: torch.Tensor         # [R + 1] int32: destination r's run starts here
+    num_experts: int
+    num_ranks: int
+    workspace: torch.Tensor | None = None
+    sched: torch.Tensor | None = None  # the local combine's counters (as Layout.sched)
+
+    @property
+    def slot(self) -> torch.Tensor:  # dispatch and combine read the send slots as slots
+        return self.send_slot
+
+
+def alloc_shard_layout(num_tokens: int, num_experts: int, num_ranks: int,
+                       device: torch.device) -> ShardLayout:
+    T, R, E = num_tokens, num_ranks, num_experts
+    i32 = dict(dtype=torch.int32, device=device)
+    ws = torch.empty(max(int(lib().ep_shard_workspace_bytes(T, R, E)), 16), dtype=torch.uint8,
+                     device=device)
+    return ShardLayout(torch.empty(R, **i32), torch.empty(E, **i32),
+                       torch.empty((T, R), dtype=torch.bool, device=device),
+                       torch.empty((T, R), **i32), torch.empty(R + 1, **i32), E, R, ws,
+                       alloc_combine_sched(device))
+
+
+def shard_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int, *,
+                 err: torch.Tensor | None = None, out: ShardLayout | None = None) -> ShardLayout:
+    """One rank's layout of its own tokens over num_ranks destinations (any
+    number of tokens): its send buffer is packed destination-major in token
+    order.  Enqueued on the current stream."""
+    _need(topk_idx, "topk_idx", torch.int64)
+    if topk_idx.dim() != 2:
+        raise EPError("topk_idx must be [num_tokens, num_topk]")
+    T, K = topk_idx.shape
+    L = out if out is not None else alloc_shard_layout(T, num_experts, num_ranks,
+                                                       topk_idx.device)
+    if err is not None:
+        _need(err, "err", torch.int32)
+    _check(lib().ep_shard_layout(_ptr(topk_idx), T, K, num_experts, num_ranks,
+                                 _ptr(L.send_counts), _ptr(L.expert_counts),
+                                 _ptr(L.is_token_in_rank), _ptr(L.send_slot), _ptr(L.send_base),
+                                 _ptr(err), _ptr(L.workspace), L.workspace.numel(),
+                                 _stream(topk_idx.device)), "ep_shard_layout")
+    _debug_check("shard_layout", err, topk_idx.device)
+    return L
+
+
+def shard_offsets(counts: np.ndarray, rank: int) -> tuple[np.ndarray, np.ndarray]:
+    """Host: from the gathered counts [R, R] (counts[s][r] = tokens of rank s
+    sent to rank r), this rank's send offsets (its runs in its send buffer)
+    and receive offsets (where each source's run lands), both [R + 1] int64."""
+    c = np.ascontiguousarray(counts, dtype=np.int32)
+    R = c.shape[0]
+    if c.shape != (R, R):
+        raise EPError("counts must be [R, R]")
+    send = np.empty(R + 1, np.int64)
+    recv = np.empty(R + 1, np.int64)
+    _check(lib().ep_shard_offsets(c.ctypes.data, R, rank, send.ctypes.data, recv.ctypes.data),
+           "ep_shard_offsets")
+    return send, recv
+
+
+def shard_recv_tokens_per_expert(expert_counts: np.ndarray, rank: int) -> np.ndarray:
+    """Host: from every rank's expert counts [R, E], the rows this rank
+    receives per local expert, [E / R] int32."""
+    c = np.ascontiguousarray(expert_counts, dtype=np.int32)
+    R, E = c.shape
+    out = np.empty(E // R if R and E % R == 0 else 0, np.int32)
+    _check(lib().ep_shard_recv_tokens_per_expert(c.ctypes.data, E, R, rank, out.ctypes.data),
+           "ep_shard_recv_tokens_per_expert")
     return out
 
 

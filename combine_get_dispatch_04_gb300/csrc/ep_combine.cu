@@ -617,7 +617,7 @@ ep_status_t combine_rank_major(const void* y, int hidden, const int64_t* topk_id
                                const float* topk_weights, int64_t num_tokens, int num_topk,
                                int num_experts, int num_ranks, const int32_t* slot, void* out,
                                uint64_t* sched, int32_t* err_word, ep_stream_t stream) {
-  if (!routing_ok(num_tokens, num_topk, num_experts, num_ranks)) return EP_ERR_INVALID_ARG;
+  if (!routing_ok_any_t(num_tokens, num_topk, num_experts, num_ranks)) return EP_ERR_INVALID_ARG;
   if (hidden < 8 || hidden % 8 != 0) return EP_ERR_INVALID_ARG;
   if (num_tokens == 0) return EP_OK;
   if (!y || !topk_idx || !slot || !out) return EP_ERR_INVALID_ARG;

@@ -36,12 +36,17 @@ struct DeviceProps {
 // Cached per device; returns false if the CUDA runtime cannot be queried.
 bool device_props(DeviceProps* out);
 
-// Common argument checks for the routing description.
-inline bool routing_ok(int64_t T, int K, int E, int R) {
+// Common argument checks for the routing description; the layout also needs
+// T % R == 0 (routing_ok), dispatch and combine do not (routing_ok_any_t):
+// there the slots, not the source ranks, place the rows.
+inline bool routing_ok_any_t(int64_t T, int K, int E, int R) {
   if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS) return false;
-  if (R < 1 || R > EP_MAX_RANKS || E % R != 0 || T % R != 0) return false;
+  if (R < 1 || R > EP_MAX_RANKS || E % R != 0) return false;
   if (T * (int64_t)R >= (int64_t(1) << 31)) return false;
   return true;
+}
+inline bool routing_ok(int64_t T, int K, int E, int R) {
+  return routing_ok_any_t(T, K, E, R) && T % R == 0;
 }
 
 // Launch with programmatic dependent launch (PDL): the kernel may be

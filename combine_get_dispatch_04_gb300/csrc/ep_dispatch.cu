@@ -91,7 +91,7 @@ extern "C" ep_status_t ep_dispatch(const void* x, int hidden, const int64_t* top
                                    int64_t* recv_topk_idx, float* recv_topk_weights,
                                    int32_t* num_recv_tokens_per_expert, int32_t* err_word,
                                    ep_stream_t stream) {
-  if (!routing_ok(num_tokens, num_topk, num_experts, num_ranks)) return EP_ERR_INVALID_ARG;
+  if (!routing_ok_any_t(num_tokens, num_topk, num_experts, num_ranks)) return EP_ERR_INVALID_ARG;
   if (hidden < 8 || hidden % 8 != 0 || (use_fp8 && hidden % 128 != 0)) return EP_ERR_INVALID_ARG;
   if (recv_capacity_rows < 0) return EP_ERR_INVALID_ARG;
   if (num_tokens > 0) {

@@ -37,8 +37,9 @@ constexpr int kTokWarps = kTok / 32;
 struct Geom {
   int64_t T, Tr;
   int K, E, El, R;
+  int S;     // source ranks: R for one call over every rank's tokens, 1 for one shard's
   int nbps;  // blocks per source rank
-  int nb;    // total blocks = R * nbps
+  int nb;    // total blocks = S * nbps
 };
 
 struct Workspace {
@@ -49,16 +50,17 @@ struct Workspace {
   size_t bytes;
 };
 
-Geom make_geom(int64_t T, int K, int E, int R) {
+Geom make_geom(int64_t T, int K, int E, int R, int S) {
   Geom g;
   g.T = T;
-  g.Tr = T / R;
+  g.S = S;
+  g.Tr = T / S;
   g.K = K;
   g.E = E;
   g.El = E / R;
   g.R = R;
   g.nbps = (int)((g.Tr + kTok - 1) / kTok);
-  g.nb = R * g.nbps;
+  g.nb = S * g.nbps;
   return g;
 }
 
@@ -178,12 +180,12 @@ __global__ void __launch_bounds__(kScanThreads)
   const int nwarps = kScanThreads / 32;
 
   // tokens of source s sent to r: sum of the blocks of s
-  for (int i = threadIdx.x; i < g.R * g.R; i += kScanThreads) {
+  for (int i = threadIdx.x; i < g.S * g.R; i += kScanThreads) {
     const int s = i / g.R, r = i % g.R;
     ntpr[i] = strided_sum(ws.blk_rank + (int64_t)r * g.nb + (int64_t)s * g.nbps, g.nbps, 1);
   }
   // slots of source s naming expert e
-  for (int64_t i = threadIdx.x; i < (int64_t)g.R * g.E; i += kScanThreads) {
+  for (int64_t i = threadIdx.x; i < (int64_t)g.S * g.E; i += kScanThreads) {
     const int s = (int)(i / g.E), e = (int)(i % g.E);
     ntpe[i] = strided_sum(ws.blk_expert + (int64_t)s * g.nbps * g.E + e, g.nbps, g.E);
   }
@@ -278,7 +280,7 @@ __global__ void __launch_bounds__(kTok)
     }
     __syncthreads();
     // this block's share of the per-source totals and of recv_base
-    const int64_t n_rank = (int64_t)g.R * g.R, n_exp = (int64_t)g.R * g.E;
+    const int64_t n_rank = (int64_t)g.S * g.R, n_exp = (int64_t)g.S * g.E;
     const int64_t n_out = n_rank + n_exp + g.R + 1;
     for (int64_t i = (int64_t)b * kTok + threadIdx.x; i < n_out; i += (int64_t)g.nb * kTok) {
       if (i < n_rank) {
@@ -621,7 +623,7 @@ using namespace ep;
 
 extern "C" size_t ep_workspace_bytes(int64_t num_tokens, int num_ranks, int num_experts) {
   if (!routing_ok(num_tokens, 1, num_experts, num_ranks)) return 0;
-  const Geom g = make_geom(num_tokens, 1, num_experts, num_ranks);
+  const Geom g = make_geom(num_tokens, 1, num_experts, num_ranks, num_ranks);
   return carve(g, nullptr).bytes;
 }
 
@@ -654,7 +656,7 @@ extern "C" ep_status_t ep_get_dispatch_layout_path(
       return EP_ERR_INVALID_ARG;
     if (!single && (!workspace || !aligned16(workspace))) return EP_ERR_INVALID_ARG;
   }
-  const Geom g = make_geom(num_tokens, num_topk, num_experts, num_ranks);
+  const Geom g = make_geom(num_tokens, num_topk, num_experts, num_ranks, num_ranks);
   const Workspace ws = carve(g, workspace);
   if (single) {
     if (launch_layout_cluster(topk_idx, g, num_tokens_per_rank, num_tokens_per_expert,
@@ -752,7 +754,7 @@ extern "C" ep_status_t ep_get_dispatch_layout_noalloc(
     if (!aligned16(slot) || !aligned16(is_token_in_rank) || !aligned16(topk_idx))
       return EP_ERR_INVALID_ARG;
   }
-  const Geom g = make_geom(num_tokens, num_topk, num_experts, num_ranks);
+  const Geom g = make_geom(num_tokens, num_topk, num_experts, num_ranks, num_ranks);
   if (carve(g, nullptr).bytes > (size_t)EP_NOALLOC_SCRATCH_BYTES) return EP_ERR_CAPACITY;
   void* scratch = nullptr;
   const ep_status_t s = noalloc_scratch(&scratch);
@@ -761,4 +763,84 @@ extern "C" ep_status_t ep_get_dispatch_layout_noalloc(
   launch_layout(topk_idx, g, ws, num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank,
                 slot, recv_base, err_word, to_cuda(stream));
   return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// Sharded form: one rank's layout of its own tokens, and the host-side
+// offsets of the exchange.
+//
+// "[Not ready] MSCCLPP EP implementation" (mscclpp pull request 852):
+// section "Scope", Intranode (get_dispatch_layout on each rank, then the
+// dispatch over peer buffers) and the internode notify_dispatch commit (the
+// count exchange that fixes the receiver-side prefix matrices).  Each rank
+// lays out its own T tokens as the one source of a layout with R
+// destinations: its send buffer is packed destination-major in token order,
+// so the rows for destination r are one contiguous run.  After an all-gather
+// of every rank's per-destination counts, each destination receives the
+// runs in source-rank order, which gives exactly the rows of the
+// single-call layout's destination r.
+// ---------------------------------------------------------------------------
+extern "C" size_t ep_shard_workspace_bytes(int64_t num_tokens, int num_ranks, int num_experts) {
+  if (!routing_ok_any_t(num_tokens, 1, num_experts, num_ranks)) return 0;
+  const Geom g = make_geom(num_tokens, 1, num_experts, num_ranks, 1);
+  return carve(g, nullptr).bytes;
+}
+
+extern "C" ep_status_t ep_shard_layout(const int64_t* topk_idx, int64_t num_tokens, int num_topk,
+                                       int num_experts, int num_ranks, int32_t* send_counts,
+                                       int32_t* expert_counts, uint8_t* is_token_in_rank,
+                                       int32_t* send_slot, int32_t* send_base,
+                                       int32_t* err_word, void* workspace,
+                                       size_t workspace_bytes, ep_stream_t stream) {
+  // one source: T need not be a multiple of R
+  if (!routing_ok_any_t(num_tokens, num_topk, num_experts, num_ranks)) return EP_ERR_INVALID_ARG;
+  if (!send_counts || !expert_counts || !send_base) return EP_ERR_INVALID_ARG;
+  const Geom g = make_geom(num_tokens, num_topk, num_experts, num_ranks, 1);
+  const Workspace ws = carve(g, workspace);
+  if (num_tokens > 0) {
+    if (!topk_idx || !is_token_in_rank || !send_slot || !workspace) return EP_ERR_INVALID_ARG;
+    if (!aligned16(send_slot) || !aligned16(is_token_in_rank) || !aligned16(topk_idx) ||
+        !aligned16(workspace))
+      return EP_ERR_INVALID_ARG;
+    if (workspace_bytes < ws.bytes) return EP_ERR_CAPACITY;
+  }
+  launch_layout(topk_idx, g, ws, send_counts, expert_counts, is_token_in_rank, send_slot,
+                send_base, err_word, to_cuda(stream));
+  return launch_status();
+}
+
+extern "C" ep_status_t ep_shard_offsets(const int32_t* counts, int num_ranks, int rank,
+                                        int64_t* send_offsets, int64_t* recv_offsets) {
+  if (!counts || !send_offsets || !recv_offsets || num_ranks < 1 || num_ranks > EP_MAX_RANKS ||
+      rank < 0 || rank >= num_ranks)
+    return EP_ERR_INVALID_ARG;
+  const int R = num_ranks;
+  send_offsets[0] = 0;
+  recv_offsets[0] = 0;
+  for (int i = 0; i < R; ++i) {
+    const int32_t out = counts[(size_t)rank * R + i];  // this rank's tokens sent to rank i
+    const int32_t in = counts[(size_t)i * R + rank];   // rank i's tokens sent to this rank
+    if (out < 0 || in < 0) return EP_ERR_INVALID_ARG;
+    send_offsets[i + 1] = send_offsets[i] + out;
+    recv_offsets[i + 1] = recv_offsets[i] + in;
+  }
+  return EP_OK;
+}
+
+extern "C" ep_status_t ep_shard_recv_tokens_per_expert(const int32_t* expert_counts,
+                                                       int num_experts, int num_ranks, int rank,
+                                                       int32_t* out) {
+  if (!expert_counts || !out || num_ranks < 1 || num_ranks > EP_MAX_RANKS || num_experts < 1 ||
+      num_experts > EP_MAX_EXPERTS || num_experts % num_ranks != 0 || rank < 0 ||
+      rank >= num_ranks)
+    return EP_ERR_INVALID_ARG;
+  const int El = num_experts / num_ranks;
+  for (int j = 0; j < El; ++j) {
+    int64_t sum = 0;
+    for (int s = 0; s < num_ranks; ++s)
+      sum += expert_counts[(size_t)s * num_experts + (size_t)rank * El + j];
+    if (sum > INT32_MAX) return EP_ERR_INVALID_ARG;
+    out[j] = (int32_t)sum;
+  }
+  return EP_OK;
 }

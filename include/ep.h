@@ -234,6 +234,8 @@ ep_status_t ep_layout_total_rows(const int32_t* recv_base, int num_ranks, int32_
  *   Rows >= P are not touched.
  * recv_capacity_rows: rows the caller allocated; a pair whose slot is >= it
  *   is skipped and sets EP_ERRBIT_CAPACITY in err_word.
+ * T need not be a multiple of R here (the slots place the rows), so the
+ * sharded form below dispatches one rank's own tokens with this call.
  */
 ep_status_t ep_dispatch(const void* x, int hidden, const int64_t* topk_idx,
                         const float* topk_weights, int64_t num_tokens, int num_topk,
@@ -266,7 +268,7 @@ ep_status_t ep_dispatch(const void* x, int hidden, const int64_t* topk_idx,
  *   (skipped), EP_ERRBIT_TIMEOUT if a bounded pipeline wait ran out (the
  *   output is then incomplete).
  * y rows are staged through shared memory with 1-D bulk (TMA) copies; y and
- * out must not overlap.
+ * out must not overlap.  T need not be a multiple of R here.
  */
 ep_status_t ep_combine(const void* y, int hidden, const int64_t* topk_idx,
                        const float* topk_weights, int64_t num_tokens, int num_topk,
@@ -335,6 +337,73 @@ ep_status_t ep_layout_dispatch_fused(
  * nothing, and still returns its state to zero.  One-shot; 0 cancels it.
  */
 void ep_debug_set_fused_stall(int on);
+
+/* ------------------------------------------------------------------------
+ * Sharded form: one process and one GPU per rank ("[Not ready] MSCCLPP EP
+ * implementation", section "Scope", Intranode: get_dispatch_layout on every
+ * rank, then dispatch and combine over peer buffers; the internode
+ * notify_dispatch commit: the count exchange that fixes the receiver-side
+ * prefix matrices).  Rank s holds its own T tokens.  Per rank:
+ *   1. ep_shard_layout: the rank's tokens as the one source of a layout
+ *      with R destinations.  Its send buffer is packed destination-major in
+ *      token order: destination r's rows are [send_base[r], send_base[r+1]).
+ *   2. an all-gather of every rank's send_counts row gives counts [R, R]
+ *      (counts[s][r] = tokens of rank s sent to rank r); ep_shard_offsets
+ *      turns it into this rank's send and receive offsets.
+ *   3. ep_dispatch with slot = send_slot (T need not be a multiple of R)
+ *      fills the send buffer; an all-to-all-v moves run r to rank r, which
+ *      stores the runs in source-rank order at its receive offsets.  Those
+ *      are exactly the rows that destination r holds in the single-call
+ *      layout (rows ordered by source rank, then token).  recv_src_idx then
+ *      holds each row's token index within its source rank.
+ *   4. combine: the reverse all-to-all-v brings every row back into the
+ *      send buffer's layout, and ep_combine with slot = send_slot reduces it.
+ * The collectives are the caller's (the Python package uses
+ * torch.distributed); the library computes the layout, the offsets and the
+ * rows.
+ * ------------------------------------------------------------------------ */
+
+/* Device scratch for ep_shard_layout (0 for invalid sizes). */
+size_t ep_shard_workspace_bytes(int64_t num_tokens, int num_ranks, int num_experts);
+
+/*
+ * The layout of one rank's T tokens (any T >= 0) over R destinations.
+ * In (device): topk_idx [T, K] int64.
+ * Out (device), every element written:
+ *   send_counts   [R] int32: tokens sent to each destination
+ *   expert_counts [E] int32: slots naming each expert
+ *   is_token_in_rank [T, R] uint8, send_slot [T, R] int32 (-1: not sent)
+ *   send_base [R + 1] int32: exclusive prefix of send_counts
+ * err_word, workspace (ep_shard_workspace_bytes), errors: as
+ * ep_get_dispatch_layout.  Always the multi-launch kernels.
+ */
+ep_status_t ep_shard_layout(const int64_t* topk_idx, int64_t num_tokens, int num_topk,
+                            int num_experts, int num_ranks, int32_t* send_counts,
+                            int32_t* expert_counts, uint8_t* is_token_in_rank,
+                            int32_t* send_slot, int32_t* send_base, int32_t* err_word,
+                            void* workspace, size_t workspace_bytes, ep_stream_t stream);
+
+/*
+ * Host function (no GPU work).  counts (host) [R, R] int32: counts[s][r] =
+ * tokens of rank s sent to rank r (every rank's send_counts, gathered).
+ * Out (host): send_offsets [R + 1] int64, the exclusive prefix of
+ * counts[rank][.] (this rank's runs in its send buffer); recv_offsets
+ * [R + 1] int64, the exclusive prefix of counts[.][rank] (where the run
+ * from each source rank lands in this rank's receive buffer;
+ * recv_offsets[R] = rows received).  EP_ERR_INVALID_ARG for a negative
+ * count or a rank outside [0, R).
+ */
+ep_status_t ep_shard_offsets(const int32_t* counts, int num_ranks, int rank,
+                             int64_t* send_offsets, int64_t* recv_offsets);
+
+/*
+ * Host function (no GPU work).  expert_counts (host) [R, E] int32: every
+ * rank's expert_counts row, gathered.  Out (host) [E/R] int32: the rows
+ * this rank receives for each of its local experts (summed over sources),
+ * the rank's row of ep_dispatch's num_recv_tokens_per_expert.
+ */
+ep_status_t ep_shard_recv_tokens_per_expert(const int32_t* expert_counts, int num_experts,
+                                            int num_ranks, int rank, int32_t* out);
 
 /* ------------------------------------------------------------------------
  * Low-latency (expert-major) layout: the receive layout of the low-latency

@@ -587,7 +587,10 @@ def time_e2e(run: StepRunner, args, case, world: int) -> dict:
     chunks: routing in -> layout; then per chunk, x in (copy stream) ->
     dispatch + combine of that chunk's tokens (compute stream) -> out back
     (second copy stream).  Every step moves all inputs in and the whole
-    result out.  Consecutive steps overlap their copies chunk by chunk."""
+    result out.  The device-side routing, x and out are double-buffered by
+    step parity and the routing travels on the input copy stream, so that
+    one step's copies wait only on the kernels of the step before the
+    previous one: neither copy direction waits behind the other's step."""
     import torch
     import torch.distributed as dist
     dev, stream, T, H = run.dev, run.stream, run.T, run.cfg.hidden
@@ -600,46 +603,60 @@ def time_e2e(run: StepRunner, args, case, world: int) -> dict:
     bounds = [T * i // n_chunks for i in range(n_chunks + 1)]
     chunks = [(bounds[c], bounds[c + 1]) for c in range(n_chunks)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(n_chunks)]      # x chunk landed
-    ev_used = [torch.cuda.Event() for _ in range(n_chunks)]    # x chunk read by dispatch
-    ev_done = [torch.cuda.Event() for _ in range(n_chunks)]    # out chunk computed
-    ev_back = [torch.cuda.Event() for _ in range(n_chunks)]    # out chunk copied back
-    x_dst = [run.x[a:b] for a, b in chunks]
-    x_src = [h_x[a:b] for a, b in chunks]
-    o_dst = [h_out[a:b] for a, b in chunks]
-    o_src = [run.out[a:b] for a, b in chunks]
-    first = [True]
+    # buffers of parity 0 are the runner's own; parity 1 a second set
+    bufs = [(run.idx, run.w, run.x, run.out),
+            (torch.empty_like(run.idx), torch.empty_like(run.w), torch.empty_like(run.x),
+             torch.empty_like(run.out))]
+    E = lambda: [torch.cuda.Event() for _ in range(n_chunks)]  # noqa: E731
+    ev_route = [torch.cuda.Event(), torch.cuda.Event()]  # routing landed, per parity
+    ev_in = [E(), E()]       # x chunk landed
+    ev_used = [E(), E()]     # x chunk read by dispatch
+    ev_done = [E(), E()]     # out chunk computed
+    ev_back = [E(), E()]     # out chunk copied back
+    ev_step = [torch.cuda.Event(), torch.cuda.Event()]  # the step's last kernel (routing free)
+    used = [False, False]
+    step_no = [0]
 
     def e2e_step():
-        # routing in and layout on the compute stream (after the previous
-        # step's kernels, which read idx and w)
-        run.idx.copy_(h_idx, non_blocking=True)
-        run.w.copy_(h_w, non_blocking=True)
+        par = step_no[0] & 1
+        idx, w, x, out = bufs[par]
+        run.idx, run.w, run.x, run.out = idx, w, x, out
         with torch.cuda.stream(s_in):
-            for c in range(n_chunks):
-                if not first[0]:
-                    s_in.wait_event(ev_used[c])  # the previous step has read this x chunk
-                x_dst[c].copy_(x_src[c], non_blocking=True)
-                ev_in[c].record(s_in)
+            if used[par]:
+                s_in.wait_event(ev_step[par])  # the routing of two steps back is no longer read
+            idx.copy_(h_idx, non_blocking=True)
+            w.copy_(h_w, non_blocking=True)
+            ev_route[par].record(s_in)
+            for c, (a, b) in enumerate(chunks):
+                if used[par]:
+                    s_in.wait_event(ev_used[par][c])
+                x[a:b].copy_(h_x[a:b], non_blocking=True)
+                ev_in[par][c].record(s_in)
+        stream.wait_event(ev_route[par])
         run.do_layout()
         for c, (a, b) in enumerate(chunks):
-            stream.wait_event(ev_in[c])
+            stream.wait_event(ev_in[par][c])
             run.do_dispatch(a, b)
-            ev_used[c].record(stream)
-            if not first[0]:
-                stream.wait_event(ev_back[c])  # the previous step's copy of this out chunk is done
+            ev_used[par][c].record(stream)
+            if used[par]:
+                stream.wait_event(ev_back[par][c])  # this buffer's copy of two steps back is done
             run.do_combine(a, b)
-            ev_done[c].record(stream)
+            ev_done[par][c].record(stream)
             with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_done[c])
-                o_dst[c].copy_(o_src[c], non_blocking=True)
-                ev_back[c].record(s_out)
-        first[0] = False
+                s_out.wait_event(ev_done[par][c])
+                h_out[a:b].copy_(out[a:b], non_blocking=True)
+                ev_back[par][c].record(s_out)
+        ev_step[par].record(stream)
+        used[par] = True
+        step_no[0] += 1
 
     def e2e_drain():
-        for c in range(n_chunks):
-            stream.wait_event(ev_back[c])
+        for par in (0, 1):
+            if used[par]:
+                for c in range(n_chunks):
+                    stream.wait_event(ev_back[par][c])
 
+    e2e_step()
     e2e_step()
     e2e_drain()
     torch.cuda.synchronize(dev)
@@ -657,11 +674,13 @@ def time_e2e(run: StepRunner, args, case, world: int) -> dict:
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / steps, dev)
     # the pipelined steps must give the resident step's result, bit for bit
+    run.idx, run.w, run.x, run.out = bufs[0]
     run.step()
     torch.cuda.synchronize(dev)
     same = torch.equal(h_out.view(torch.int16), run.out.cpu().view(torch.int16))
     h2d = h_idx.numel() * 8 + h_w.numel() * 4 + h_x.numel() * 2
     d2h = h_out.numel() * 2
+    del bufs
     link = link_bandwidth(dev)
     floor_ms = 1e3 * max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9),
                          (h2d + d2h) / (link["both_gbs"] * 1e9))
@@ -853,6 +872,81 @@ def run_ours(args, cfg: Config):
         dist.destroy_process_group()
 
 
+def run_sharded(args, cfg: Config):
+    """The sharded form under torchrun, one rank per GPU: every rank holds the
+    workload's tokens_per_rank tokens, the experts are spread over the N
+    ranks, and one step is shard layout -> count exchange -> dispatch ->
+    all-to-all-v -> (identity experts) -> reverse all-to-all-v -> combine
+    (combine_get_dispatch_04_gb300.sharded).  value = N * T_r / the slowest
+    rank's step time."""
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist.init_process_group("nccl", device_id=dev)
+    import combine_get_dispatch_04_gb300 as ep
+    from combine_get_dispatch_04_gb300 import build as ep_build
+    from combine_get_dispatch_04_gb300 import sharded
+    from dataclasses import replace
+    if not ep_build.up_to_date():
+        raise SystemExit("libep.so is missing or stale: run __graft_entry__.build() first")
+    ep.load()
+    if cfg.num_experts % world:
+        raise SystemExit(f"{cfg.num_experts} experts do not spread over {world} ranks")
+    gcfg = replace(cfg, num_ranks=world)  # the same routing recipe over `world` ranks
+    case = make_case(gcfg)
+    Tr = gcfg.tokens_per_rank
+    a, b = rank * Tr, (rank + 1) * Tr
+    idx = torch.from_numpy(np.ascontiguousarray(case.topk_idx[a:b])).to(dev)
+    w = torch.from_numpy(np.ascontiguousarray(case.topk_weights[a:b])).to(dev)
+    x = torch.from_numpy(np.ascontiguousarray(case.x_bits[a:b]).view(np.int16)).view(
+        torch.bfloat16).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    sep = sharded.ShardedEP(sharded.DistExchange())
+
+    def step():
+        recv, handle = sep.dispatch(x, idx, w, gcfg.num_experts, use_fp8=gcfg.fp8, err=err)
+        y = recv.recv_x if not gcfg.fp8 else torch.ones(
+            (recv.recv_x.shape[0], gcfg.hidden), dtype=torch.bfloat16, device=dev)
+        return sep.combine(y, handle, err=err)
+
+    for _ in range(args.warmup):
+        out = step()
+    torch.cuda.synchronize(dev)
+    if not bool(torch.isfinite(out.float()).all()):
+        raise SystemExit("combine produced a non-finite value")
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    if int(err.item()) != 0:
+        raise SystemExit(f"device error word {int(err.item())}")
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": whole_job_tokens_per_s(Tr, world, ms), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3+bf16" if gcfg.fp8 else "bf16",
+            "data": "synthetic (seeded routing and N(0,1) hidden states; no dataset)",
+            "config": dict(workload=cfg.name, tokens_per_rank=Tr, num_ranks=world,
+                           hidden=gcfg.hidden, num_experts=gcfg.num_experts,
+                           num_topk=gcfg.num_topk, parallelism=f"ep{world} sharded",
+                           steps_include="count exchange with a host copy, all-to-all-v both ways"),
+            # per step: the shard layout (count + assign, or + scan), dispatch, combine
+            "gpu_launches": (2 + (world * ((Tr + 511) // 512) > 8192) + 2) * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -875,6 +969,10 @@ def main(argv=None):
                     help="time the plain steps as replays of one CUDA graph of the step "
                          "(no host launch cost; the per-kernel pass stays eager)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sharded", action="store_true",
+                    help="under torchrun: the sharded form, one rank per GPU with the "
+                         "workload's tokens per rank (the default --gpus N run is N "
+                         "independent replicas of the one-GPU shuffle)")
     ap.add_argument("--workloads", dest="workloads", action="store_true", default=None,
                     help="also time the other workloads (default: on for the default run)")
     ap.add_argument("--no-workloads", dest="workloads", action="store_false")
@@ -900,6 +998,8 @@ def main(argv=None):
         cfg = replace(cfg, seed=args.seed)
     if args.impl == "reference":
         run_reference(args, cfg)
+    elif args.sharded:
+        run_sharded(args, cfg)
     else:
         run_ours(args, cfg)
 

@@ -111,10 +111,14 @@ def load_traffic(kernel: str, workload: str):
         parts = dict(p.split("=", 1) for p in line.split())
         if parts.get("kernel") != kernel or parts.get("workload") != workload:
             continue
-        src = os.path.join(ROOT, "combine_get_dispatch_04_gb300", "csrc", parts["source"])
-        if not os.path.exists(src):
-            return None
-        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != parts["sha"]:
+        # source: the kernel's files, '+'-separated, hashed in that order
+        h = hashlib.sha256()
+        for name in parts["source"].split("+"):
+            src = os.path.join(ROOT, "combine_get_dispatch_04_gb300", "csrc", name)
+            if not os.path.exists(src):
+                return None
+            h.update(open(src, "rb").read())
+        if h.hexdigest()[:16] != parts["sha"]:
             return None
         return float(parts["dram_bytes_per_launch"])
     return None
@@ -826,7 +830,7 @@ def run_ours(args, cfg: Config):
         kern["combine"]["launches_per_step"] = 1
         dom = "dispatch" if kern["dispatch"]["ms"] >= kern["combine"]["ms"] else "combine"
         kname = {"dispatch": "dispatch_kernel", "combine": "combine_kernel"}[dom]
-        src = {"dispatch": "ep_dispatch.cu", "combine": "ep_combine.cu"}[dom]
+        src = {"dispatch": "ep_dispatch.cu+ep_scatter.cuh", "combine": "ep_combine.cu"}[dom]
         # expert-major runs have their own captures ("<workload>/ll")
         traffic = load_traffic(kname, cfg.name + ("/ll" if args.layout == "ll" else ""))
         cpu = None if (args.no_cpu_baseline or world > 1 or args.layout == "ll") else cpu_baseline(case)

@@ -77,3 +77,4 @@ def test_bench_workloads_block(ep):
         assert w[k]["frac"] == pytest.approx(w[k]["gbs"] / d["peak_gbs"])
     assert w["l2"].startswith("flushed")  # x (58.7 MB) fits in L2
     assert w["clocks"]["samples"] >= 1 and w["dtype"] == "e4m3+bf16"
+    assert w["step_launch"] == "eager"  # only a step that fits in L2 replays as a graph

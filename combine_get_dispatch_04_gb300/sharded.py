@@ -88,11 +88,18 @@ class DistExchange:
 
 
 def _row_bytes(t: torch.Tensor) -> torch.Tensor:
-    """The same memory as [rows, bytes per row] uint8 (contiguous t)."""
+    """The same memory as [rows, bytes per row] uint8.  t must be contiguous
+    (a received run must land in t itself, not in a copy); an empty t, which
+    may carry any strides, becomes an empty byte tensor of the same width."""
     inner = 1
     for d in t.shape[1:]:
         inner *= int(d)
-    return t.reshape(t.shape[0], inner).view(torch.uint8)
+    if t.numel() == 0:
+        return torch.empty((t.shape[0], inner * t.element_size()), dtype=torch.uint8,
+                           device=t.device)
+    if not t.is_contiguous():
+        raise EPError("the exchange needs contiguous row buffers")
+    return t.view(t.shape[0], inner).view(torch.uint8)
 
 
 @dataclass

@@ -78,3 +78,16 @@ def test_bench_workloads_block(ep):
     assert w["l2"].startswith("flushed")  # x (58.7 MB) fits in L2
     assert w["clocks"]["samples"] >= 1 and w["dtype"] == "e4m3+bf16"
     assert w["step_launch"] == "eager"  # only a step that fits in L2 replays as a graph
+
+
+def test_bench_sharded_line_under_torchrun(ep):
+    """The sharded form's bench line, one rank (NCCL, world size 1: the
+    all-to-all is a copy to itself)."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "1",
+           "--master-addr", "127.0.0.1", "--master-port", "29633", os.path.join(ROOT, "bench.py"),
+           "--sharded", "--config", "decode_fp8", "--steps", "3", "--warmup", "3"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][0])
+    assert d["n_gpus"] == 1 and d["value"] > 0 and d["config"]["parallelism"] == "ep1 sharded"
+    assert d["config"]["tokens_per_rank"] == 128 and d["gpu_launches"] > 0

@@ -66,7 +66,9 @@ def _rank_main(rank, world, port, outdir, fp8):
     sys.path.insert(0, root)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     import torch.distributed as dist
-    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from datetime import timedelta
+    # a rank that fails makes the others' collectives raise, not wait forever
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=timedelta(seconds=60))
     result = {"ok": False}
     try:
         import oracle
@@ -124,8 +126,10 @@ def _rank_main(rank, world, port, outdir, fp8):
     finally:
         with open(os.path.join(outdir, f"rank{rank}.json"), "w") as f:
             json.dump(result, f)
-        dist.barrier()
-        dist.destroy_process_group()
+        try:
+            dist.barrier()
+        finally:
+            dist.destroy_process_group()
 
 
 @pytest.mark.parametrize("world,fp8", [(2, False), (4, False), (2, True), (4, True)])
@@ -150,3 +154,83 @@ def test_shard_offsets_host_function():
         ep.shard_offsets(np.array([[1, -1], [0, 0]], np.int32), 0)
     per = ep.shard_recv_tokens_per_expert(np.arange(12, dtype=np.int32).reshape(2, 6), 1)
     assert per.tolist() == [3 + 9, 4 + 10, 5 + 11]  # experts 3..5 of rank 1, summed over sources
+
+
+def _rank_main_unequal(rank, world, port, outdir):
+    """Ranks with different numbers of tokens (rank 1 has none): each
+    destination's received rows against a brute-force assembly of the runs
+    (for every source rank in order, its tokens sent to the destination in
+    token order), and the combined tokens against the oracle's combine of the
+    rank's own tokens over the rows it gets back."""
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    from datetime import timedelta
+    # a rank that fails makes the others' collectives raise, not wait forever
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=timedelta(seconds=60))
+    result = {"ok": False}
+    try:
+        import oracle
+        from combine_get_dispatch_04_gb300 import sharded
+        R, E, K, H = world, 6 * world, 3, 64
+        counts = [23, 0, 41][:world]
+        rng = np.random.default_rng(77)  # the same draws on every rank
+        idx_all = [np.argsort(rng.random((n, E)), axis=1)[:, :K].astype(np.int64) for n in counts]
+        for a in idx_all:
+            a[rng.random(a.shape) < 0.2] = -1
+        w_all = [rng.random((n, K)).astype(np.float32) for n in counts]
+        x_all = [rng.integers(0, 1 << 16, (n, H), dtype=np.uint16) & 0xBFFF for n in counts]
+        me = rank
+        ep = sharded.ShardedEP(sharded.DistExchange(), OracleSteps())
+        recv, handle = ep.dispatch(torch.from_numpy(x_all[me].view(np.int16)),
+                                   torch.from_numpy(idx_all[me]), torch.from_numpy(w_all[me]), E)
+        El = E // R
+        want_rows, want_src = [], []
+        for s in range(R):
+            for t in range(counts[s]):
+                ranks = {int(e) // El for e in idx_all[s][t] if e >= 0}
+                if me in ranks:
+                    want_rows.append(x_all[s][t])
+                    want_src.append(t)
+        got = recv.recv_x.numpy().view(np.uint16)
+        assert got.shape[0] == len(want_rows)
+        if want_rows:
+            np.testing.assert_array_equal(got, np.stack(want_rows))
+            np.testing.assert_array_equal(recv.recv_src_idx.numpy(), np.array(want_src))
+        np.testing.assert_array_equal(np.diff(recv.recv_offsets),
+                                      [sum(1 for t in range(counts[s])
+                                           if me in {int(e) // El for e in idx_all[s][t] if e >= 0})
+                                       for s in range(R)])
+        # experts: every received row doubled (exact in bf16)
+        y = torch.from_numpy((got.astype(np.uint32) + (1 << 7)).astype(np.uint16).view(np.int16)) \
+            if got.size else torch.empty((0, H), dtype=torch.int16)
+        out = ep.combine(y, handle)
+        sl = oracle.shard_layout(idx_all[me], E, R)
+        back = np.zeros((int(sl.send_base[-1]), H), np.uint16)
+        for t in range(counts[me]):
+            for r in range(R):
+                if sl.send_slot[t, r] >= 0:
+                    back[sl.send_slot[t, r]] = (x_all[me][t].astype(np.uint32) + (1 << 7)).astype(np.uint16)
+        want = oracle.combine(back, idx_all[me], w_all[me], E, R, sl.send_slot)
+        np.testing.assert_array_equal(out.numpy().view(np.uint16), want)
+        result = {"ok": True}
+    except Exception:
+        result = {"ok": False, "error": traceback.format_exc()}
+    finally:
+        with open(os.path.join(outdir, f"rank{rank}.json"), "w") as f:
+            json.dump(result, f)
+        try:
+            dist.barrier()
+        finally:
+            dist.destroy_process_group()
+
+
+def test_sharded_exchange_with_unequal_and_empty_ranks(tmp_path):
+    import torch.multiprocessing as mp
+    world = 3
+    mp.spawn(_rank_main_unequal, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    for i in range(world):
+        r = json.load(open(tmp_path / f"rank{i}.json"))
+        assert r["ok"], f"rank {i}:\n{r.get('error')}"

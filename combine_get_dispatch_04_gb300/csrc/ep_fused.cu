@@ -41,12 +41,14 @@
 // EP_ERRBIT_TIMEOUT; the blocks then skip their scatter and leave.
 //
 // Measured on one GB300 against ep_get_dispatch_layout followed by
-// ep_dispatch (each kernel timed alone, L2 flushed before it): 8192 tokens at
-// 8 ranks, 7168 bf16 channels, top-8 of 256 experts: 119.9 us against
-// 13.5 + 113.2 us; 512 tokens at 4 ranks: 17.1 us against 10.4 + 9.5 us; but
-// the 4096-token FP8 decode batch at 32 ranks: 66 us against 12.6 + 45.6 us.
-// There the layout takes about 10 us of the launch (its exchanges go through
-// L2 under the scatter's load), and the 3584 short blocks each pay for a
+// ep_dispatch, per layout -> dispatch -> combine step: 16384 tokens at 8
+// ranks, 7168 bf16 channels, top-8 of 256 experts: 450.2 against 455.0 us
+// (8192 tokens: 238.4 against 240.1 us); but every smaller batch is slower
+// fused: the 4096-token FP8 decode batch at 32 ranks 150.7 against 135.5 us,
+// 512 tokens at 4 ranks 27.6 against 23.9 us.  The layout phase takes about
+// 10 us of the launch (its exchanges go through L2 under the other blocks'
+// loads) and overlaps with nothing, whereas two launches overlap the layout
+// with the dispatch's launch; and each of many short blocks pays for a
 // ticket, a flag poll and an exit count on shared counters.
 #include <mutex>
 
@@ -110,12 +112,13 @@ struct LayoutSmem {
 };
 
 // Phase A for warp `warp` of the layout block with ticket k: one 32-token
-// group.  Returns the lane's rank mask (0 for lanes past the source's end).
-__device__ __forceinline__ uint64_t layout_group(const FusedArgs& f, int k, int warp, int lane,
-                                                 bool& bad) {
+// group's is_token_in_rank rows and its ballots (lanes past the source's end
+// vote for nothing).
+__device__ __forceinline__ void layout_group(const FusedArgs& f, int k, int warp, int lane,
+                                             bool& bad) {
   const ScatterArgs& a = f.s;
   const int g = k * kFWarps + warp;
-  if (g >= f.W) return 0;
+  if (g >= f.W) return;  // uniform per warp
   const int s = g / f.gps, gl = g % f.gps;
   const int64_t tl = (int64_t)gl * 32 + lane;
   const bool valid = tl < f.Tr;
@@ -157,7 +160,6 @@ __device__ __forceinline__ uint64_t layout_group(const FusedArgs& f, int k, int 
   }
   if (lane < a.R) f.bal[(int64_t)g * a.R + lane] = b0;
   if (lane + 32 < a.R) f.bal[(int64_t)g * a.R + lane + 32] = b1;
-  return mask;
 }
 
 // Ballots each thread of a layout block loads in phase B: the whole table,

@@ -3,7 +3,9 @@
  * Two ranks, 8 tokens (4 per rank), 4 experts (2 per rank), top-2.  The
  * expected layout is worked out by hand below; dispatch must copy each token
  * to its slots, and combine with identity experts and weights 0.5 + 0.5 must
- * return x exactly.  Prints "ok" and exits 0 on success.
+ * return x exactly.  The sharded form's layout of one rank's tokens and its
+ * host offsets are worked out by hand too.  Prints "ok" and exits 0 on
+ * success.
  */
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -116,6 +118,48 @@ int main(void) {
     CUDA(cudaMemcpy(sched, d_sched, sizeof sched, cudaMemcpyDeviceToHost));
     CHECK(memcmp(out2, out, sizeof out) == 0, "scheduled combine");
     CHECK(sched[0] == 0 && sched[1] == 0, "counters back to zero");
+  }
+
+  /* the sharded form: rank 1 of 2 holds tokens 4..7 and lays them out alone.
+     By hand: token 4 -> rank 0, 5 -> rank 1, 6 -> nowhere, 7 -> ranks 0 and 1,
+     so its send buffer is [4, 7 | 5, 7]. */
+  {
+    enum { TS = 4 };
+    int32_t *d_cnt, *d_ecnt, *d_sslot, *d_sbase;
+    uint8_t* d_sin;
+    void* d_sws;
+    const size_t sws = ep_shard_workspace_bytes(TS, R, E);
+    CHECK(sws > 0, "shard workspace size");
+    CUDA(cudaMalloc((void**)&d_cnt, sizeof(int32_t) * R));
+    CUDA(cudaMalloc((void**)&d_ecnt, sizeof(int32_t) * E));
+    CUDA(cudaMalloc((void**)&d_sslot, sizeof(int32_t) * TS * R));
+    CUDA(cudaMalloc((void**)&d_sbase, sizeof(int32_t) * (R + 1)));
+    CUDA(cudaMalloc((void**)&d_sin, (size_t)TS * R));
+    CUDA(cudaMalloc(&d_sws, sws));
+    EP(ep_shard_layout(d_idx + 4 * K, TS, K, E, R, d_cnt, d_ecnt, d_sin, d_sslot, d_sbase, d_err,
+                       d_sws, sws, NULL));
+    int32_t sslot[TS][R], sbase[R + 1], cnt[R], ecnt[E];
+    CUDA(cudaMemcpy(sslot, d_sslot, sizeof sslot, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(sbase, d_sbase, sizeof sbase, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(cnt, d_cnt, sizeof cnt, cudaMemcpyDeviceToHost));
+    CUDA(cudaMemcpy(ecnt, d_ecnt, sizeof ecnt, cudaMemcpyDeviceToHost));
+    const int32_t want_sslot[TS][R] = {{0, -1}, {-1, 2}, {-1, -1}, {1, 3}};
+    const int32_t want_sbase[R + 1] = {0, 2, 4}, want_cnt[R] = {2, 2}, want_ecnt[E] = {2, 1, 1, 1};
+    CHECK(memcmp(sslot, want_sslot, sizeof sslot) == 0, "send slots");
+    CHECK(memcmp(sbase, want_sbase, sizeof sbase) == 0, "send_base");
+    CHECK(memcmp(cnt, want_cnt, sizeof cnt) == 0, "send counts");
+    CHECK(memcmp(ecnt, want_ecnt, sizeof ecnt) == 0, "expert counts");
+    /* rank 0 (tokens 0..3) sends 2 tokens to itself and 3 to rank 1 */
+    const int32_t counts[R][R] = {{2, 3}, {2, 2}};
+    int64_t so[R + 1], ro[R + 1];
+    EP(ep_shard_offsets(&counts[0][0], R, 1, so, ro));
+    CHECK(so[0] == 0 && so[1] == 2 && so[2] == 4, "send offsets");
+    /* rank 1 receives rank 0's 3 rows, then its own 2: rows 4..8 of the single-call layout */
+    CHECK(ro[0] == 0 && ro[1] == 3 && ro[2] == 5, "receive offsets");
+    const int32_t ec[R][E] = {{2, 1, 2, 2}, {2, 1, 1, 1}};
+    int32_t per[E / R];
+    EP(ep_shard_recv_tokens_per_expert(&ec[0][0], E, R, 1, per));
+    CHECK(per[0] == 3 && per[1] == 3, "per-expert receive counts");
   }
 
   printf("ok\n");

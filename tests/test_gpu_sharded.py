@@ -159,3 +159,18 @@ def test_sharded_ranks_on_one_gpu_match_the_single_call_oracle(ep, cfg):
         np.testing.assert_array_equal(recv.num_recv_tokens_per_expert, nrpe[rank])
         a, b = rank * Tr, (rank + 1) * Tr
         assert_combine_close(bits_of(out), want_out[a:b], bound[a:b])
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_sharded_random_shapes(ep, i):
+    """The random sweep's generator, kept to at most 16 ranks (one host thread
+    each): bf16 rows, and FP8 where H % 128 == 0."""
+    from test_gpu_random import random_config
+    j = i
+    cfg = random_config(j)
+    while cfg.num_ranks > 16:  # the next shapes of the same sweep
+        j += 100
+        cfg = random_config(j)
+    for fp8 in ([False, True] if cfg.hidden % 128 == 0 else [False]):
+        c = cfg.__class__(**{**cfg.__dict__, "fp8": fp8})
+        test_sharded_ranks_on_one_gpu_match_the_single_call_oracle(ep, c)

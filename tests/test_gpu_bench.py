@@ -42,6 +42,9 @@ def test_bench_line_on_the_small_workload(ep, layout, graph):
     assert e2e["check"] == "out matches the device-resident step"
     assert e2e["link"]["h2d_gbs"] > 0 and e2e["link"]["d2h_gbs"] > 0
     assert 0 < e2e["link_floor_ms"] and e2e["host_enqueue_ms_per_step"] > 0
+    # the reported end-to-end step is the median of its timed passes
+    assert len(e2e["passes_ms"]) == 3
+    assert sorted(e2e["passes_ms"])[1] == pytest.approx(e2e["ms_per_step"], abs=1e-3)
     # one single-launch layout, dispatch and combine per step, in every timed pass
     assert d["passes"]["n"] >= 1 and d["passes"]["steps_each"] == 5
     assert d["passes"]["ms_min"] <= d["ms_per_step"] <= d["passes"]["ms_max"]

@@ -42,10 +42,10 @@
 //
 // Measured on one GB300 against ep_get_dispatch_layout followed by
 // ep_dispatch, per layout -> dispatch -> combine step: 16384 tokens at 8
-// ranks, 7168 bf16 channels, top-8 of 256 experts: 450.2 against 455.0 us
-// (8192 tokens: 238.4 against 240.1 us); but every smaller batch is slower
-// fused: the 4096-token FP8 decode batch at 32 ranks 150.7 against 135.5 us,
-// 512 tokens at 4 ranks 27.6 against 23.9 us.  The layout phase takes about
+// ranks, 7168 bf16 channels, top-8 of 256 experts: 448.5 against 450.7 us
+// (8192 tokens: 238.0 against 237.5 us); every smaller batch is slower
+// fused: the 4096-token FP8 decode batch at 32 ranks 150.3 against 133.5 us,
+// 512 tokens at 4 ranks 27.0 against 23.4 us.  The layout phase takes about
 // 10 us of the launch (its exchanges go through L2 under the other blocks'
 // loads) and overlaps with nothing, whereas two launches overlap the layout
 // with the dispatch's launch; and each of many short blocks pays for a

@@ -668,8 +668,10 @@ def time_e2e(run: StepRunner, args, case, world: int) -> dict:
                 for c in range(n_chunks):
                     stream.wait_event(ev_back[par][c])
 
-    e2e_step()
-    e2e_step()
+    # warm-up: one untimed pass (the first pass after only two steps often
+    # read slower than the ones after it)
+    for _ in range(max(2, steps)):
+        e2e_step()
     e2e_drain()
     torch.cuda.synchronize(dev)
     if world > 1:

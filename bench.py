@@ -677,8 +677,7 @@ def time_e2e(run: StepRunner, args, case, world: int) -> dict:
     if world > 1:
         dist.barrier()
     # Passes of `steps` steps each, the median pass reported (as for the
-    # device time): the copies share the host's memory and link with other
-    # processes, and a pass now and then reads up to 40% slower.
+    # device time), after the untimed pass above.
     pass_ms, host_s = [], 0.0
     for _ in range(E2E_PASSES):
         e0 = torch.cuda.Event(enable_timing=True)

@@ -1,4 +1,4 @@
-"""Randomised parity sweep (48 cases; EP_RANDOM_CASES=n for more): many
+"""Randomised parity sweep (256 cases; EP_RANDOM_CASES=n for more): many
 small seeded shapes (ranks 1..64, ragged tokens per rank, 1..8 experts per
 rank, top-1..12, hidden sizes from one 16-byte vector up, uniform or Zipf
 routing, 0-50% masked slots), each run through every entry point and
@@ -21,7 +21,7 @@ from workloads import Config, make_case
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = int(os.environ.get("EP_RANDOM_CASES", "48"))
+N_CASES = int(os.environ.get("EP_RANDOM_CASES", "256"))
 
 
 def random_config(i: int) -> Config:

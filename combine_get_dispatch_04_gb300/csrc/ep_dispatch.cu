@@ -104,10 +104,14 @@ extern "C" ep_status_t ep_dispatch(const void* x, int hidden, const int64_t* top
   if (hidden < 8 || hidden % 8 != 0 || (use_fp8 && hidden % 128 != 0)) return EP_ERR_INVALID_ARG;
   if (recv_capacity_rows < 0) return EP_ERR_INVALID_ARG;
   if (num_tokens > 0) {
-    if (!x || !topk_idx || !slot || !recv_x) return EP_ERR_INVALID_ARG;
+    if (!x || !topk_idx || !slot) return EP_ERR_INVALID_ARG;
     if ((recv_topk_idx || recv_topk_weights) && !topk_weights) return EP_ERR_INVALID_ARG;
-    if (use_fp8 && !recv_scales) return EP_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(recv_x)) return EP_ERR_INVALID_ARG;
+    if (!aligned16(x)) return EP_ERR_INVALID_ARG;
+  }
+  // with no receive rows nothing is written (every slot is out of capacity),
+  // so the receive buffers may then be NULL
+  if (num_tokens > 0 && recv_capacity_rows > 0) {
+    if (!recv_x || (use_fp8 && !recv_scales) || !aligned16(recv_x)) return EP_ERR_INVALID_ARG;
   }
   if (num_recv_tokens_per_expert && !num_tokens_per_expert) return EP_ERR_INVALID_ARG;
   Args a = {};
@@ -144,8 +148,10 @@ extern "C" ep_status_t ep_ll_dispatch(const void* x, int hidden, int64_t num_tok
   if (hidden < 8 || hidden % 8 != 0 || (use_fp8 && hidden % 128 != 0)) return EP_ERR_INVALID_ARG;
   if (recv_capacity_rows < 0 || recv_capacity_rows >= (int64_t(1) << 31)) return EP_ERR_INVALID_ARG;
   if (num_tokens > 0) {
-    if (!x || !ll_slot || !recv_x || (use_fp8 && !recv_scales)) return EP_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(recv_x)) return EP_ERR_INVALID_ARG;
+    if (!x || !ll_slot || !aligned16(x)) return EP_ERR_INVALID_ARG;
+  }
+  if (num_tokens > 0 && recv_capacity_rows > 0) {  // no receive rows: nothing is written
+    if (!recv_x || (use_fp8 && !recv_scales) || !aligned16(recv_x)) return EP_ERR_INVALID_ARG;
   }
   Args a = {};
   a.x = static_cast<const int4*>(x);

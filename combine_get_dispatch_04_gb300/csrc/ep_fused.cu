@@ -464,13 +464,15 @@ extern "C" ep_status_t ep_layout_dispatch_fused(
   if (hidden < 8 || hidden % 8 != 0 || (use_fp8 && hidden % 128 != 0)) return EP_ERR_INVALID_ARG;
   if (recv_capacity_rows < 0) return EP_ERR_INVALID_ARG;
   if (!x || !topk_idx || !num_tokens_per_rank || !num_tokens_per_expert || !is_token_in_rank ||
-      !slot || !recv_base || !recv_x || !workspace || !sync)
+      !slot || !recv_base || !workspace || !sync)
     return EP_ERR_INVALID_ARG;
   if ((recv_topk_idx || recv_topk_weights) && !topk_weights) return EP_ERR_INVALID_ARG;
-  if (use_fp8 && !recv_scales) return EP_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(recv_x) || !aligned16(slot) || !aligned16(is_token_in_rank) ||
+  if (!aligned16(x) || !aligned16(slot) || !aligned16(is_token_in_rank) ||
       !aligned16(workspace) || (reinterpret_cast<uintptr_t>(sync) & 7) != 0)
     return EP_ERR_INVALID_ARG;
+  if (recv_capacity_rows > 0) {  // no receive rows: nothing is written, the buffers may be NULL
+    if (!recv_x || (use_fp8 && !recv_scales) || !aligned16(recv_x)) return EP_ERR_INVALID_ARG;
+  }
   const int R = num_ranks;
   const int64_t Tr = num_tokens / R;
   const int gps = (int)((Tr + 31) / 32);

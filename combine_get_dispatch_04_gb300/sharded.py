@@ -202,7 +202,11 @@ class ShardedEP:
         plan = handle.plan
         if y.shape[0] < plan.recv_rows:
             raise EPError(f"y must have the {plan.recv_rows} received rows, got {y.shape[0]}")
-        back = torch.empty((plan.send_rows, y.shape[1]), dtype=y.dtype, device=y.device)
-        self.ex.all_to_all_rows(back, y[:plan.recv_rows], plan.send_splits, plan.recv_splits)
+        # A rank that sent no rows (every one of its slots masked) still runs
+        # the combine, which writes its zero rows and reads no row of y: one
+        # placeholder row keeps y a real buffer.
+        back = torch.empty((max(plan.send_rows, 1), y.shape[1]), dtype=y.dtype, device=y.device)
+        self.ex.all_to_all_rows(back[:plan.send_rows], y[:plan.recv_rows], plan.send_splits,
+                                plan.recv_splits)
         w = handle.topk_weights if weighted else None
         return self.steps.combine(back, handle.topk_idx, w, handle.layout, err=err)

@@ -233,7 +233,9 @@ ep_status_t ep_layout_total_rows(const int32_t* recv_base, int num_ranks, int32_
  *   destination rank receives per local expert, summed over source ranks.
  *   Rows >= P are not touched.
  * recv_capacity_rows: rows the caller allocated; a pair whose slot is >= it
- *   is skipped and sets EP_ERRBIT_CAPACITY in err_word.
+ *   is skipped and sets EP_ERRBIT_CAPACITY in err_word.  With 0 rows nothing
+ *   is written, and recv_x / recv_scales may be NULL (a shard whose tokens
+ *   all go nowhere has an empty send buffer).
  * T need not be a multiple of R here (the slots place the rows), so the
  * sharded form below dispatches one rank's own tokens with this call.
  */
@@ -480,7 +482,7 @@ ep_status_t ep_ll_get_dispatch_layout_path(const int64_t* topk_idx, int64_t num_
  * In (device): x [T, H] bf16, ll_slot [T, K].  Out (device): recv_x
  * [capacity, H] (bf16 or bytes), recv_scales [capacity, H/128] f32 (FP8),
  * recv_src_idx [capacity] int32.  Rows >= recv_capacity_rows are skipped
- * and set EP_ERRBIT_CAPACITY.
+ * and set EP_ERRBIT_CAPACITY; with 0 rows recv_x / recv_scales may be NULL.
  */
 ep_status_t ep_ll_dispatch(const void* x, int hidden, int64_t num_tokens, int num_topk,
                            const int32_t* ll_slot, int64_t recv_capacity_rows, int use_fp8,

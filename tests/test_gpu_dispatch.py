@@ -143,6 +143,36 @@ def test_dispatch_empty(ep):
     assert not out.num_recv_tokens_per_expert.any()
 
 
+def test_dispatch_with_no_receive_rows(ep):
+    """Tokens whose slots are all masked, into buffers of no rows (NULL
+    pointers): every dispatch entry point writes nothing and reports nothing
+    (a shard whose tokens all go nowhere has such an empty send buffer); one
+    live slot with no rows to hold it sets the capacity bit."""
+    T, H, K, E, R = 64, 256, 2, 8, 4
+    idx = torch.full((T, K), -1, dtype=torch.int64, device="cuda")
+    w = torch.rand((T, K), device="cuda")
+    x = torch.randn((T, H), device="cuda").to(torch.bfloat16)
+    for fp8 in (False, True):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        L = ep.get_dispatch_layout(idx, E, R)
+        d = ep.dispatch(x, idx, w, L, use_fp8=fp8, capacity=0, err=err)
+        assert d.recv_x.data_ptr() == 0
+        L2, d2 = ep.layout_dispatch(x, idx, w, E, R, use_fp8=fp8, capacity=0, err=err)
+        LL = ep.ll_get_dispatch_layout(idx, E, R, 0, err=err)
+        dl = ep.ll_dispatch(x, LL, use_fp8=fp8, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, fp8
+        assert dl.recv_x.shape[0] == 0 and d2.recv_x.shape[0] == 0
+        assert not d.num_recv_tokens_per_expert.any() and not d2.num_recv_tokens_per_expert.any()
+        assert not L2.num_tokens_per_rank.any()
+    idx[5, 0] = 3
+    L = ep.get_dispatch_layout(idx, E, R)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.dispatch(x, idx, w, L, capacity=0, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == ep.EP_ERRBIT_CAPACITY
+
+
 @pytest.mark.parametrize("name", ["tiny", "dsv3_prefill", "skewed", "mixtral"])
 def test_dispatch_bf16_full_size(ep, name):
     """Full-size bf16 workloads in the benchmark's launch configuration

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from ep_testlib import bits_of, device_inputs, fp8_small_configs, small_configs
-from test_gpu_random import random_config
+from test_gpu_random import N_CASES, random_config
 from workloads import CONFIGS, make_case
 
 pytestmark = pytest.mark.gpu
@@ -86,7 +86,7 @@ def test_fused_small_fp8(ep, cfg):
     check_fused(ep, cfg, make_case(cfg), use_fp8=True)
 
 
-@pytest.mark.parametrize("i", range(48))
+@pytest.mark.parametrize("i", range(N_CASES))
 def test_fused_random_shape(ep, i):
     cfg = random_config(i)
     if not ep.fused_fits(cfg.num_tokens, cfg.num_ranks, cfg.num_experts):

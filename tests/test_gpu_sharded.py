@@ -10,6 +10,8 @@ and scales, metadata, per-expert counts), and its combined tokens the
 single-call oracle combine within the combine tolerance."""
 from __future__ import annotations
 
+import os
+
 import threading
 
 import numpy as np
@@ -82,9 +84,18 @@ class ThreadExchange:
         self._sync()
 
 
-def run_ranks(ep, cfg, fp8, y_global):
+def masked_case(cfg, masked_ranks=(), with_hidden=True):
+    """The workload's case, with every slot of the tokens of masked_ranks set to -1."""
+    c = make_case(cfg, with_hidden=with_hidden)
+    Tr = cfg.tokens_per_rank
+    for r in masked_ranks:
+        c.topk_idx[r * Tr:(r + 1) * Tr] = -1
+    return c
+
+
+def run_ranks(ep, cfg, fp8, y_global, masked_ranks=()):
     from combine_get_dispatch_04_gb300 import sharded
-    c = make_case(cfg)
+    c = masked_case(cfg, masked_ranks)
     R, Tr, E = cfg.num_ranks, cfg.tokens_per_rank, cfg.num_experts
     shared = {"barrier": threading.Barrier(R), "rows": [None] * R, "a2a": [None] * R}
     results, errors = [None] * R, []
@@ -130,11 +141,24 @@ def run_ranks(ep, cfg, fp8, y_global):
     Config("shard_gpu_decode", 8, 128, 7168, 64, 8, fp8=True, seed=4102),
 ], ids=lambda c: c.name)
 def test_sharded_ranks_on_one_gpu_match_the_single_call_oracle(ep, cfg):
+    check_sharded_against_single_call(ep, cfg)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_sharded_rank_with_every_slot_masked(ep, fp8):
+    """A rank whose tokens all go nowhere sends no rows: its dispatch writes
+    into an empty send buffer and its combine reads no row (all its tokens
+    come back as zeros); the other ranks still exchange with it."""
+    cfg = Config("shard_gpu_masked_rank", 4, 96, 256, 16, 4, fp8=fp8, seed=4103)
+    check_sharded_against_single_call(ep, cfg, masked_ranks=(1,))
+
+
+def check_sharded_against_single_call(ep, cfg, masked_ranks=()):
     R, Tr, E, H = cfg.num_ranks, cfg.tokens_per_rank, cfg.num_experts, cfg.hidden
-    c0 = make_case(cfg, with_hidden=False)
+    c0 = masked_case(cfg, masked_ranks, with_hidden=False)
     P = oracle.layout(c0.topk_idx, E, R).num_rows
     Y = workloads.expert_outputs(P, H, seed=cfg.seed + 9)
-    c, G, results = run_ranks(ep, cfg, cfg.fp8, Y)
+    c, G, results = run_ranks(ep, cfg, cfg.fp8, Y, masked_ranks)
     gd = oracle.dispatch(c.x_bits, c.topk_idx, c.topk_weights, E, R, G.slot, P, use_fp8=cfg.fp8)
     nrpe = oracle.num_recv_tokens_per_expert(G.num_tokens_per_expert, E, R)
     want_out = oracle.combine(Y, c.topk_idx, c.topk_weights, E, R, G.slot)
@@ -161,7 +185,7 @@ def test_sharded_ranks_on_one_gpu_match_the_single_call_oracle(ep, cfg):
         assert_combine_close(bits_of(out), want_out[a:b], bound[a:b])
 
 
-@pytest.mark.parametrize("i", range(8))
+@pytest.mark.parametrize("i", range(int(os.environ.get("EP_SHARDED_CASES", "64"))))
 def test_sharded_random_shapes(ep, i):
     """The random sweep's generator, kept to at most 16 ranks (one host thread
     each): bf16 rows, and FP8 where H % 128 == 0."""

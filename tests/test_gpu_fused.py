@@ -15,6 +15,7 @@ import torch
 import oracle
 from ep_testlib import bits_of, device_inputs, fp8_small_configs, small_configs
 from test_gpu_random import N_CASES, random_config
+from test_gpu_adversarial import CASES as _ADV, _case as _adv_case
 from workloads import CONFIGS, make_case
 
 pytestmark = pytest.mark.gpu
@@ -167,3 +168,16 @@ def test_fused_wait_runs_out_then_recovers(ep):
     assert (bits_of(D.recv_x) == 0xFFFF).all()  # nothing dispatched
     assert not L.fused_sync.any()
     check_fused(ep, cfg, c, use_fp8=False)
+
+
+@pytest.mark.parametrize("i", range(len(_ADV)), ids=lambda i: "{}-{}".format(_ADV[i][0], _ADV[i][1][0]))
+def test_fused_adversarial_routing(ep, i):
+    """The adversarial routings (duplicate experts, bad ids, one hot expert or
+    rank, masked tokens) through the one-launch layout + dispatch."""
+    kind, shape = _ADV[i]
+    cfg, c = _adv_case(kind, shape, i)
+    if not ep.fused_fits(cfg.num_tokens, cfg.num_ranks, cfg.num_experts):
+        pytest.skip("outside the one-launch limits")
+    check_fused(ep, cfg, c, use_fp8=False)
+    if cfg.hidden % 128 == 0:
+        check_fused(ep, cfg, c, use_fp8=True)

@@ -21,6 +21,7 @@ import torch
 import oracle
 import workloads
 from ep_testlib import assert_combine_close, bits_of, combine_bound
+from test_gpu_adversarial import CASES as _ADV, _case as _adv_case
 from workloads import Config, make_case
 
 pytestmark = pytest.mark.gpu
@@ -84,18 +85,21 @@ class ThreadExchange:
         self._sync()
 
 
-def masked_case(cfg, masked_ranks=(), with_hidden=True):
-    """The workload's case, with every slot of the tokens of masked_ranks set to -1."""
+def masked_case(cfg, masked_ranks=(), with_hidden=True, routing=None):
+    """The workload's case (with the given top-k ids instead of its own, if
+    any), with every slot of the tokens of masked_ranks set to -1."""
     c = make_case(cfg, with_hidden=with_hidden)
+    if routing is not None:
+        c.topk_idx[:] = routing
     Tr = cfg.tokens_per_rank
     for r in masked_ranks:
         c.topk_idx[r * Tr:(r + 1) * Tr] = -1
     return c
 
 
-def run_ranks(ep, cfg, fp8, y_global, masked_ranks=()):
+def run_ranks(ep, cfg, fp8, y_global, masked_ranks=(), routing=None):
     from combine_get_dispatch_04_gb300 import sharded
-    c = masked_case(cfg, masked_ranks)
+    c = masked_case(cfg, masked_ranks, routing=routing)
     R, Tr, E = cfg.num_ranks, cfg.tokens_per_rank, cfg.num_experts
     shared = {"barrier": threading.Barrier(R), "rows": [None] * R, "a2a": [None] * R}
     results, errors = [None] * R, []
@@ -153,19 +157,20 @@ def test_sharded_rank_with_every_slot_masked(ep, fp8):
     check_sharded_against_single_call(ep, cfg, masked_ranks=(1,))
 
 
-def check_sharded_against_single_call(ep, cfg, masked_ranks=()):
+def check_sharded_against_single_call(ep, cfg, masked_ranks=(), routing=None):
     R, Tr, E, H = cfg.num_ranks, cfg.tokens_per_rank, cfg.num_experts, cfg.hidden
-    c0 = masked_case(cfg, masked_ranks, with_hidden=False)
+    c0 = masked_case(cfg, masked_ranks, with_hidden=False, routing=routing)
     P = oracle.layout(c0.topk_idx, E, R).num_rows
-    Y = workloads.expert_outputs(P, H, seed=cfg.seed + 9)
-    c, G, results = run_ranks(ep, cfg, cfg.fp8, Y, masked_ranks)
+    Y = workloads.expert_outputs(max(P, 1), H, seed=cfg.seed + 9)
+    c, G, results = run_ranks(ep, cfg, cfg.fp8, Y, masked_ranks, routing)
     gd = oracle.dispatch(c.x_bits, c.topk_idx, c.topk_weights, E, R, G.slot, P, use_fp8=cfg.fp8)
     nrpe = oracle.num_recv_tokens_per_expert(G.num_tokens_per_expert, E, R)
     want_out = oracle.combine(Y, c.topk_idx, c.topk_weights, E, R, G.slot)
     bound = combine_bound(oracle.bf16_to_double(Y), c.topk_idx, c.topk_weights, G.slot, E // R,
                           np.arange(cfg.num_tokens))
     for rank, (recv, out, err) in enumerate(results):
-        assert err == 0
+        # bad ids in the rank's own tokens, as its shard layout reports them
+        assert err == oracle.shard_layout(c.topk_idx[rank * Tr:(rank + 1) * Tr], E, R).err_bits
         lo, hi = int(G.recv_base[rank]), int(G.recv_base[rank + 1])
         if cfg.fp8:
             np.testing.assert_array_equal(recv.recv_x.cpu().numpy(), gd.recv_x[lo:hi])
@@ -198,3 +203,16 @@ def test_sharded_random_shapes(ep, i):
     for fp8 in ([False, True] if cfg.hidden % 128 == 0 else [False]):
         c = cfg.__class__(**{**cfg.__dict__, "fp8": fp8})
         test_sharded_ranks_on_one_gpu_match_the_single_call_oracle(ep, c)
+
+
+@pytest.mark.parametrize("i", [i for i, (_, shape) in enumerate(_ADV) if shape[1] <= 16],
+                         ids=lambda i: "{}-{}".format(_ADV[i][0], _ADV[i][1][0]))
+def test_sharded_adversarial_routing(ep, i):
+    """The adversarial routings (duplicate experts, bad ids, one hot expert or
+    rank, masked tokens) through the sharded exchange, up to 16 ranks: ranks
+    that send or receive nothing included."""
+    kind, shape = _ADV[i]
+    cfg, c = _adv_case(kind, shape, i)
+    for fp8 in ([False, True] if cfg.hidden % 128 == 0 else [False]):
+        check_sharded_against_single_call(ep, cfg.__class__(**{**cfg.__dict__, "fp8": fp8}),
+                                          routing=c.topk_idx)

@@ -71,3 +71,17 @@ def test_largest_batch_the_api_takes(ep):
         assert_combine_close(out[a:b], ref, bound)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("H", [16384, 65528, 131072])
+def test_wide_rows(ep, H):
+    """Rows far wider than any workload's (up to 256 KB of bf16): many
+    chunks per row in the combine, many rounds per warp in the dispatch; FP8
+    where H % 128 == 0."""
+    from test_gpu_random import check_expert_major, check_rank_major
+    from workloads import Config, make_case
+    cfg = Config(f"wide_h{H}", 4, 16, H, 8, 3, routing="zipf", zipf_s=1.2, mask_prob=0.1,
+                 seed=9700 + H % 97)
+    c = make_case(cfg)
+    check_rank_major(ep, cfg, c)
+    check_expert_major(ep, cfg, c)

@@ -59,3 +59,14 @@ def test_whole_job_value_counts_every_replica():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.whole_job_tokens_per_s(131072, 4, 1.6) == pytest.approx(131072 * 4 / 1.6e-3)
+
+
+def test_traffic_figures_belong_to_the_current_kernels():
+    """Every entry of profiles/ncu_traffic.txt is keyed by a hash of its
+    kernel's source files: a kernel edited since its capture would make the
+    bench report roofline.traffic as null.  This keeps them in step."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for kernel in ("dispatch_kernel", "combine_kernel"):
+        for workload in ("skewed", "dsv3_prefill", "mixtral", "decode_fp8"):
+            assert bench.load_traffic(kernel, workload) is not None, (kernel, workload)

@@ -68,5 +68,6 @@ def test_traffic_figures_belong_to_the_current_kernels():
     sys.path.insert(0, ROOT)
     import bench
     for kernel in ("dispatch_kernel", "combine_kernel"):
-        for workload in ("skewed", "dsv3_prefill", "mixtral", "decode_fp8"):
+        for workload in ("skewed", "dsv3_prefill", "mixtral", "decode_fp8",
+                         "decode_fp8/ll", "dsv3_prefill/ll"):
             assert bench.load_traffic(kernel, workload) is not None, (kernel, workload)

@@ -163,7 +163,7 @@ def test_combine_full_size(ep, name):
         assert not out2[~live].view(torch.int16).any()
 
 
-@pytest.mark.parametrize("name", ["dsv3_prefill", "skewed"])
+@pytest.mark.parametrize("name", ["tiny", "dsv3_prefill", "decode_fp8", "skewed", "mixtral"])
 def test_combine_full_batch_weighted_vs_oracle(ep, name):
     """Every token of a full-size workload against the oracle, under the
     workload's own (softmax, partly masked) weights and random expert outputs,

@@ -8,8 +8,8 @@ import pytest
 import torch
 
 import oracle
-from ep_testlib import (POISON_BF16, POISON_U8, bits_of, compact_slots, device_inputs,
-                        fp8_small_configs, full_case, sample_token_ranges, small_configs)
+from ep_testlib import (POISON_BF16, POISON_U8, bits_of, device_inputs, fp8_small_configs,
+                        full_case, small_configs)
 from workloads import CONFIGS, make_case
 
 pytestmark = pytest.mark.gpu
@@ -178,8 +178,7 @@ def test_dispatch_bf16_full_size(ep, name):
     """Full-size bf16 workloads in the benchmark's launch configuration
     (worst-case capacity T*min(K,R), no synchronisation between the calls):
     every (token, rank) row is checked against the token on the device, and
-    three sampled token ranges (start, unaligned middle, ragged end) against
-    the oracle, metadata included."""
+    the whole receive buffer and its metadata against the oracle."""
     cfg = CONFIGS[name]
     c, want_layout = full_case(name)
     idx, w, x = device_inputs(c)
@@ -201,18 +200,15 @@ def test_dispatch_bf16_full_size(ep, name):
         rows = s[tok, r].long()
         assert torch.equal(out.recv_x[rows].view(torch.int16), x[t0 + tok].view(torch.int16))
         assert torch.equal(out.recv_src_idx[rows], (t0 + tok).int())
-    # sampled ranges against the oracle (rows renumbered compactly)
-    for (a, b) in sample_token_ranges(T):
-        toks = np.arange(a, b)
-        sub, orig, compact = compact_slots(slot, toks)
-        want = oracle.dispatch(c.x_bits, c.topk_idx, c.topk_weights, cfg.num_experts,
-                               cfg.num_ranks, sub, orig.size, t_range=(a, b))
-        o = torch.from_numpy(orig.astype(np.int64)).cuda()
-        np.testing.assert_array_equal(bits_of(out.recv_x[o]), want.recv_x[compact])
-        np.testing.assert_array_equal(out.recv_topk_idx[o].cpu().numpy(), want.recv_topk_idx[compact])
-        np.testing.assert_array_equal(out.recv_topk_weights[o].cpu().numpy().view(np.uint32),
-                                      want.recv_topk_weights[compact].view(np.uint32))
+    # the whole batch against the oracle
     assert P <= out.recv_x.shape[0]
+    want = oracle.dispatch(c.x_bits, c.topk_idx, c.topk_weights, cfg.num_experts,
+                           cfg.num_ranks, slot, P)
+    assert np.array_equal(bits_of(out.recv_x[:P]), want.recv_x)
+    assert np.array_equal(out.recv_src_idx[:P].cpu().numpy(), want.recv_src_idx)
+    assert np.array_equal(out.recv_topk_idx[:P].cpu().numpy(), want.recv_topk_idx)
+    assert np.array_equal(out.recv_topk_weights[:P].cpu().numpy().view(np.uint32),
+                          want.recv_topk_weights.view(np.uint32))
 
 
 def test_dispatch_fp8_every_bf16_value(ep):

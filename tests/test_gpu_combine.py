@@ -238,7 +238,8 @@ def test_combine_unweighted_rank_sum(ep, cfg):
 
 def test_combine_unweighted_full_skewed(ep):
     """Rank sum at full size (skewed workload, dispatched rows as expert
-    outputs): sampled token ranges against the oracle."""
+    outputs): every token against the oracle, the tolerance checked on the
+    device in token chunks."""
     cfg = CONFIGS["skewed"]
     c, want_layout = full_case("skewed")
     idx, w, x = device_inputs(c)
@@ -246,19 +247,21 @@ def test_combine_unweighted_full_skewed(ep):
     d = ep.dispatch(x, idx, w, L)
     out = ep.combine(d.recv_x, idx, None, L)
     torch.cuda.synchronize()
-    slot = L.slot.cpu().numpy()
-    for (a, b) in sample_token_ranges(cfg.num_tokens):
-        toks = np.arange(a, b)
-        sub, orig, compact = compact_slots(slot, toks)
-        ysub = np.empty((orig.size, cfg.hidden), np.uint16)
-        ysub[compact] = bits_of(d.recv_x[torch.from_numpy(orig.astype(np.int64)).cuda()])
-        want = oracle.combine_ranksum(ysub, sub, t_range=(a, b))[a:b]
-        yv = np.abs(oracle.bf16_to_double(ysub))
-        bound = np.zeros((b - a, cfg.hidden))
-        for r in range(cfg.num_ranks):
-            p = sub[a:b, r]
-            bound[p >= 0] += yv[p[p >= 0]]
-        assert_combine_close(bits_of(out[a:b]), want, bound)
+    P = want_layout.num_rows
+    want = oracle.combine_ranksum(bits_of(d.recv_x[:P]), want_layout.slot)
+    slot = L.slot.long()
+    T = cfg.num_tokens
+    for a in range(0, T, 2048):
+        b = min(T, a + 2048)
+        s = slot[a:b]
+        rows = d.recv_x[s.clamp(min=0)].double().abs()  # [tokens, R, H]: 1 GB
+        bound = torch.where((s >= 0)[:, :, None], rows, 0.0).sum(dim=1)
+        g = out[a:b].double()
+        r = torch.from_numpy(want[a:b].view(np.int16)).cuda().view(torch.bfloat16).double()
+        assert bool(torch.isfinite(g).all())
+        excess = (g - r).abs() - 1e-2 * (r.abs() + bound)
+        assert not bool((excess > 0).any()), (
+            f"tokens [{a}, {b}): {int((excess > 0).sum())} elements out of tolerance")
 
 
 def test_combine_bounded_wait_reports_timeout_and_recovers(ep):

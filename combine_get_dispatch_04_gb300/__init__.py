@@ -48,7 +48,7 @@ EXPORTED = ("ep_status_string", "ep_workspace_bytes", "ep_get_dispatch_layout",
             "ep_layout_dispatch_fused_fits", "ep_layout_dispatch_fused",
             "ep_layout_dispatch_fused_workspace_bytes", "ep_debug_set_fused_stall",
             "ep_shard_workspace_bytes", "ep_shard_layout", "ep_shard_offsets",
-            "ep_shard_recv_tokens_per_expert")
+            "ep_shard_recv_tokens_per_expert", "ep_debug_e4m3_range")
 
 # 64-bit words of a combine's scheduling counters (EP_COMBINE_SCHED_WORDS)
 COMBINE_SCHED_WORDS = 2
@@ -110,6 +110,7 @@ def load(path: str | None = None) -> C.CDLL:
                                            i32, P, P, P, P, P, P, P, sz, P, P, P]
     L.ep_debug_set_fused_stall.argtypes = [i32]
     L.ep_debug_set_fused_stall.restype = None
+    L.ep_debug_e4m3_range.argtypes = [C.c_uint32, i64, P, P]
     L.ep_shard_workspace_bytes.argtypes = [i64, i32, i32]
     L.ep_shard_workspace_bytes.restype = sz
     L.ep_shard_layout.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
@@ -120,7 +121,7 @@ def load(path: str | None = None) -> C.CDLL:
                  "ep_ll_get_dispatch_layout", "ep_ll_get_dispatch_layout_path",
                  "ep_ll_dispatch", "ep_ll_combine", "ep_combine_sched", "ep_ll_combine_sched",
                  "ep_layout_dispatch_fused", "ep_shard_layout", "ep_shard_offsets",
-                 "ep_shard_recv_tokens_per_expert"):
+                 "ep_shard_recv_tokens_per_expert", "ep_debug_e4m3_range"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -660,3 +661,12 @@ def ll_combine(y: torch.Tensor, topk_weights: torch.Tensor | None, layout: LLLay
            "ep_ll_combine_sched")
     _debug_check("ll_combine", err, y.device)
     return out
+
+
+def debug_e4m3_range(first: int, out: torch.Tensor) -> None:
+    """Test hook: out[i] = the FP8 dispatch's E4M3 code for the float32 with
+    bit pattern first + i (out: uint8, a multiple of 4 elements).  Enqueued on
+    the current stream."""
+    _need(out, "out", torch.uint8)
+    _check(lib().ep_debug_e4m3_range(int(first), out.numel(), _ptr(out), _stream(out.device)),
+           "ep_debug_e4m3_range")

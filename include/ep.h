@@ -553,6 +553,19 @@ ep_status_t ep_ll_combine_sched(const void* y, int hidden, const float* topk_wei
  */
 void ep_debug_set_combine_stall(int unit);
 
+/*
+ * Test hook for the FP8 payload conversion (the pages give the FP8 cast only
+ * by name, kUseFP8 in the low-latency port of "[Not ready] MSCCLPP EP
+ * implementation"; this hook has no counterpart there).  out[i] receives the
+ * E4M3 code that the FP8 dispatch's conversion (round to nearest even,
+ * saturating to +-448) gives the float32 whose bit pattern is first + i, for
+ * 0 <= i < n, so that a test can compare the oracle's encoder with the
+ * device on every float32.  n % 4 == 0 and first + n <= 2^32, else
+ * EP_ERR_INVALID_ARG; out: device, n bytes, 4-byte aligned.  Asynchronous
+ * on `stream`.
+ */
+ep_status_t ep_debug_e4m3_range(uint32_t first, int64_t n, uint8_t* out, ep_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,7 +19,7 @@ EP_ERR_CAPACITY = 2
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(ep_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(ep_[a-z0-9_]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")

@@ -230,12 +230,35 @@ def calibrate_sample(case, target_s: float) -> int:
     return int(max(1, min(case.cfg.tokens_per_rank, target_s / per_tok / case.cfg.num_ranks)))
 
 
+def host_cpu() -> dict:
+    """This host's logical cores and CPU model (lscpu, else /proc/cpuinfo)."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return {"nproc": os.cpu_count(), "model": model or platform.machine()}
+
+
 def cpu_baseline(case, target_s: float = 10.0) -> dict:
     n = calibrate_sample(case, target_s)
     sub = sub_batch(case, n)
     dt = oracle_step(sub)
     T = sub.cfg.num_tokens
-    return {"value": T / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": T / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_cpu(),
             "sample": (f"first {n} tokens of each of the {case.cfg.num_ranks} source ranks "
                        f"({T} tokens, same routing/hidden rows as the workload): layout + "
                        f"dispatch + combine, single-threaded C oracle, {dt:.2f} s")}
@@ -285,6 +308,7 @@ def run_reference(args, cfg: Config):
         "config": dict(config_dict(cfg, P, cfg.num_tokens * min(cfg.num_topk, cfg.num_ranks),
                                    cfg.num_tokens * cfg.hidden * 2), layout="ht"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "host": host_cpu(),
                          "sample": f"each step: first {n} tokens of each source rank "
                                    f"({sub.cfg.num_tokens} tokens), single-threaded C oracle"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -33,6 +33,7 @@ def test_reference_arm_prints_the_contract_line():
     assert d["config"]["workload"] == "tiny"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert cb["host"]["nproc"] >= 1 and cb["host"]["model"]
     assert cb["sample"]
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]

@@ -61,6 +61,7 @@ def test_bench_line_on_the_small_workload(ep, layout, graph):
     if layout == "ht":
         cb = d["cpu_baseline"]
         assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
+        assert cb["host"]["nproc"] >= 1 and cb["host"]["model"]
 
 
 def test_bench_workloads_block(ep):

@@ -737,6 +737,24 @@ def time_e2e(run: StepRunner, args, case, world: int) -> dict:
             "check": "out matches the device-resident step" if same else "MISMATCH"}
 
 
+def pages_convention(cfg: Config, P: int, kern: dict) -> dict:
+    """The byte accounting of the pages' own benchmarks, for context only
+    ("[Not ready] MSCCLPP EP implementation", the bench commits): the
+    dispatch counts each rank's bench_tokens * hidden, and the combine one
+    copy per dispatched row back to its owner; bandwidth is reported per rank
+    (aggregate / ranks) and aggregated.  Over all ranks of one call that is
+    T * H payload elements for the dispatch and P * H bf16 rows for the
+    combine; the roofline counts every row read and written instead."""
+    T, H, R = cfg.num_tokens, cfg.hidden, cfg.num_ranks
+    out = {"note": "dispatch: bench_tokens * hidden per rank (E4M3 bytes for the FP8 dispatch, "
+                   "else bf16); combine: one bf16 copy per dispatched row; per rank = "
+                   "aggregate / ranks; context only, not the roofline's bytes"}
+    for k, b in (("dispatch", T * H * (1 if cfg.fp8 else 2)), ("combine", P * H * 2)):
+        gbs = b / (kern[k]["ms"] / 1e3) / 1e9
+        out[k] = {"bytes": b, "aggregate_gbs": round(gbs, 1), "per_rank_gbs": round(gbs / R, 1)}
+    return out
+
+
 def kernel_report(cfg: Config, P: int, t: dict, peak: float) -> dict:
     ab = algorithmic_bytes(cfg, P)
     kern = {
@@ -901,6 +919,7 @@ def run_ours(args, cfg: Config):
                          "algorithmic_bytes_per_launch": ab[dom],
                          "peak_note": f"of {peak_kind} (copy bandwidth)"},
             "kernels": kern,
+            "pages_convention": pages_convention(cfg, P, kern),
             "passes": {"n": len(t["passes"]), "steps_each": args.steps,
                        "ms_min": min(t["passes"]), "ms_max": max(t["passes"]),
                        "note": "value and ms_per_step come from the median pass"},

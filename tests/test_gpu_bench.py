@@ -52,6 +52,13 @@ def test_bench_line_on_the_small_workload(ep, layout, graph):
     assert "workloads" not in d  # only the default run carries the other workloads
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     # per-kernel times: each kernel alone (roofline), and inside ordinary steps
+    # the pages' own accounting, for context: T * H for the dispatch, one copy
+    # per dispatched row for the combine
+    pc = d["pages_convention"]
+    assert pc["dispatch"]["bytes"] == T * H * 2
+    assert pc["combine"]["bytes"] == d["config"]["recv_rows"] * H * 2
+    assert pc["dispatch"]["per_rank_gbs"] == pytest.approx(pc["dispatch"]["aggregate_gbs"] / 4,
+                                                           abs=0.1)
     kt = d["kernel_timing"]
     assert kt["steps"] == 5 and kt["in_step_ms_per_step"] > 0
     parts = sum(kt["in_step"][k + "_ms"] for k in ("layout", "dispatch", "combine"))

@@ -254,14 +254,18 @@ def host_cpu() -> dict:
 
 
 def cpu_baseline(case, target_s: float = 10.0) -> dict:
-    n = calibrate_sample(case, target_s)
+    """The oracle's step on a bounded sample of the workload: the median of
+    three runs of about a third of target_s each."""
+    n = calibrate_sample(case, target_s / 3)
     sub = sub_batch(case, n)
-    dt = oracle_step(sub)
+    times = sorted(oracle_step(sub) for _ in range(3))
+    dt = times[1]
     T = sub.cfg.num_tokens
     return {"value": T / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_cpu(),
             "sample": (f"first {n} tokens of each of the {case.cfg.num_ranks} source ranks "
                        f"({T} tokens, same routing/hidden rows as the workload): layout + "
-                       f"dispatch + combine, single-threaded C oracle, {dt:.2f} s")}
+                       f"dispatch + combine, single-threaded C oracle, median of 3 runs "
+                       f"({', '.join(f'{v:.2f}' for v in times)} s)")}
 
 
 # ----------------------------------------------------------------------------

@@ -29,8 +29,10 @@ def _to_device(c, idx, w, x):
     x.copy_(torch.from_numpy(c.x_bits.view(np.int16)).view(torch.bfloat16))
 
 
-@pytest.mark.parametrize("path", ["single", "multi"])
+@pytest.mark.parametrize("path", ["single", "multi", "fused"])
 def test_rank_major_step_in_a_cuda_graph(ep, path):
+    """path: the layout's kernels, or "fused" for layout and dispatch in one
+    launch (whose counters must be back at zero for every replay)."""
     c0, c1 = _cases()
     cfg = c0.cfg
     T, H, K, E, R = cfg.num_tokens, cfg.hidden, cfg.num_topk, cfg.num_experts, cfg.num_ranks
@@ -44,8 +46,11 @@ def test_rank_major_step_in_a_cuda_graph(ep, path):
     D = ep.alloc_dispatched(ep.worst_case_rows(T, K, R), H, K, E, R, False, dev)
 
     def step():
-        ep.get_dispatch_layout(idx, E, R, err=err, out=L, path=path)
-        ep.dispatch(x, idx, w, L, err=err, out=D)
+        if path == "fused":
+            ep.layout_dispatch(x, idx, w, E, R, err=err, layout=L, out=D)
+        else:
+            ep.get_dispatch_layout(idx, E, R, err=err, out=L, path=path)
+            ep.dispatch(x, idx, w, L, err=err, out=D)
         ep.combine(D.recv_x, idx, w, L, err=err, out=out)
 
     _to_device(c0, idx, w, x)

@@ -810,8 +810,10 @@ def other_workloads(args, ep, dev, peak: float) -> dict:
             "ms_per_step": t["ms"], "steps": args.steps, "passes": len(t["passes"]),
             "hbm_gbs": (ab["dispatch"] + ab["combine"]) / (t["ms"] / 1e3) / 1e9,
             "layout_ms": kern["layout"]["ms"], "layout_kernels": kinds,
-            "dispatch": {k: kern["dispatch"][k] for k in ("ms", "gbs", "frac")},
-            "combine": {k: kern["combine"][k] for k in ("ms", "gbs", "frac")},
+            "dispatch": dict({k: kern["dispatch"][k] for k in ("ms", "gbs", "frac")},
+                             bytes=ab["dispatch"], traffic=load_traffic("dispatch_kernel", name)),
+            "combine": dict({k: kern["combine"][k] for k in ("ms", "gbs", "frac")},
+                            bytes=ab["combine"], traffic=load_traffic("combine_kernel", name)),
             "kernel_timing": {"in_step_ms_per_step": t["ms_kernels"],
                               "in_step": t["in_step"]},
             "recv_rows": P, "dtype": "e4m3+bf16" if cfg.fp8 else "bf16",

@@ -86,6 +86,9 @@ def test_bench_workloads_block(ep):
     assert w["ms_per_step"] > 0 and w["tokens_per_s"] == pytest.approx(4096 / (w["ms_per_step"] / 1e3))
     for k in ("dispatch", "combine"):
         assert w[k]["frac"] == pytest.approx(w[k]["gbs"] / d["peak_gbs"])
+        # DRAM bytes per launch from the captures of the current kernels, near the
+        # algorithmic bytes (short by what is still in L2 when the kernel ends)
+        assert 0.7 * w[k]["bytes"] < w[k]["traffic"] <= 1.01 * w[k]["bytes"]
     assert w["l2"].startswith("flushed")  # x (58.7 MB) fits in L2
     assert w["clocks"]["samples"] >= 1 and w["dtype"] == "e4m3+bf16"
     assert w["step_launch"] == "eager"  # only a step that fits in L2 replays as a graph

@@ -16,8 +16,9 @@
 //     is fixed; with a scheduling counter (the _sched entry points) every
 //     further batch is claimed from it with one atomic, so CTAs that the
 //     memory system serves faster take more batches and all finish within
-//     about a batch of each other.  Without it CTA b takes every grid-th
-//     batch.  The last CTA to exit returns the counter to zero.
+//     about a batch of each other.  Without it (and when every CTA has only
+//     its first batch) CTA b takes every grid-th batch.  The last CTA to
+//     exit returns the counter to zero.
 //   - warp 1 (routing): claims the next batch before it needs it, and for
 //     each batch each lane gathers one token's routing into a
 //     double-buffered table (headed by the batch's first token and size):
@@ -599,6 +600,12 @@ ep_status_t launch_combine(Args& a, const DeviceProps& props, ep_stream_t stream
   const int64_t batches = (a.T + a.claim - 1) / a.claim;
   a.nbatches = batches;
   const int64_t grid = batches < ctas ? batches : ctas;
+  // One batch per CTA leaves nothing to claim: the static schedule then
+  // spares every CTA its failed claim and its exit count on the shared
+  // counters (same-address atomics; measured on the 512-token batch: combine
+  // 12.3 -> 10.3 us, step as a CUDA-graph replay 23.7 -> 21.5 us).  The
+  // counters are left untouched.
+  if (batches <= grid) a.sched = nullptr;
   launch_pdl(kernel, (unsigned)grid, kThreads, plan.smem, to_cuda(stream), a);
   return launch_status();
 }

@@ -528,8 +528,9 @@ ep_status_t ep_ll_combine(const void* y, int hidden, const float* topk_weights,
  * output may be missing tokens.  A shared state is not always caught (a
  * launch that runs entirely between the other's claims sees nothing amiss,
  * but then neither output is affected).  A NULL sched is the static
- * schedule of ep_combine.  Other arguments and errors: as ep_combine and
- * ep_ll_combine.
+ * schedule of ep_combine.  A batch small enough that every block has only
+ * its first batch is scheduled statically too, and leaves the state
+ * untouched.  Other arguments and errors: as ep_combine and ep_ll_combine.
  * ------------------------------------------------------------------------ */
 #define EP_COMBINE_SCHED_WORDS 2
 

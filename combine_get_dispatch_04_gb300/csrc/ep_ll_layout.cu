@@ -264,6 +264,14 @@ __global__ void __launch_bounds__(kLThreads, 1)
     n = (b - a) * K;
     j0 = ((int64_t)s * Tr + a) * K;
   }
+  // the warp's first eight steps of ids, loaded before the zeroing below so
+  // that their memory latency overlaps it
+  int64_t ev0[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int j = u * 32 + lane;
+    ev0[u] = j < n ? topk_idx[j0 + j] : -1;
+  }
   for (int x = tid; x < kLWarps * E; x += kLThreads) wcnt[x] = 0;
   __syncthreads();
 
@@ -275,10 +283,15 @@ __global__ void __launch_bounds__(kLThreads, 1)
 #pragma unroll 1
   for (int j00 = 0; j00 < n; j00 += 32 * 8) {
     int64_t ev[8];  // eight steps of ids loaded before any is used
+    if (j00 == 0) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int j = j00 + u * 32 + lane;
-      ev[u] = j < n ? ids[j] : -1;
+      for (int u = 0; u < 8; ++u) ev[u] = ev0[u];
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j00 + u * 32 + lane;
+        ev[u] = j < n ? ids[j] : -1;
+      }
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
